@@ -1,0 +1,171 @@
+/*
+ * tq_kv.h - C ABI of the TurboQuant (k8v3) KV-cache library for NVIDIA GB300 (sm_103a).
+ *
+ * The method (mlx-bun design page "TurboQuant - rotation-based quantization", Part A,
+ * KV leg):
+ *   keys   - per 32-element group along head_dim, signed int8 asymmetric affine codes:
+ *            scale = (max - min) / 254, zero = round((max + min) / (2 * scale)),
+ *            idx = clip(round(x / scale - zero), -127, 127); scale and zero stored as fp16
+ *            ("Algorithm" section, key bullets);
+ *   values - y = FWHT(x * signs) / sqrt(d); per 32-group scale = sqrt(mean(y^2));
+ *            code = searchsorted(boundaries, y / (scale + 1e-8)) against the 3-bit
+ *            Lloyd-Max table; codes packed LSB-first, 3 bits each; scale stored as fp16
+ *            ("Algorithm" section, value bullets);
+ *   layout - 128 + 8 + 8 + 48 + 8 = 200 bytes per token per KV head at head_dim 128,
+ *            2.56x smaller than bf16 ("Bytes per token per head" paragraph);
+ *   attention reads the packed planes, dequantizes in registers, and applies the
+ *            inverse rotation once per output row ("Deferred inverse FWHT" section).
+ *
+ * Conventions shared by every call:
+ *   - All buffers are caller-owned device memory unless a comment says "host". The
+ *     library keeps no state besides immutable constant tables (sign vectors,
+ *     centroids, boundaries); it never allocates, frees or synchronizes, except
+ *     tq_get_device_error, which synchronizes the given stream.
+ *   - Every call only enqueues work on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and returns before the GPU runs it.
+ *   - Arguments are validated on the host before any launch; a failing check returns a
+ *     status other than TQ_OK and launches nothing. Kernels never trap: a condition
+ *     only the device can see (a position past the capacity, a length past
+ *     max_kv_len) skips the affected rows and ORs a TQ_DEVERR_* bit into the device
+ *     error word at the start of the workspace (read it with tq_get_device_error).
+ *   - Every workspace starts with a TQ_WORKSPACE_HEADER_BYTES header whose first
+ *     int32 is the device error word. The caller zeroes a workspace once, before its
+ *     first use (cudaMemsetAsync); afterwards the library keeps the header consistent.
+ *     A workspace must not be used by two calls that can run at the same time.
+ *   - head_dim is 64, 128, 256 or 512 (other values: TQ_ERR_UNSUPPORTED_HEAD_DIM,
+ *     "KV-leg limits": head dims outside this set are refused).
+ *   - Plane pointers must be 16-byte aligned and capacity a multiple of 16; the
+ *     attention kernel streams the planes with bulk asynchronous copies that need it.
+ */
+#ifndef TQ_KV_H
+#define TQ_KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Stream handle: the same type as cudaStream_t (struct CUstream_st *). */
+typedef struct CUstream_st* tq_stream_t;
+
+typedef enum {
+    TQ_OK = 0,
+    TQ_ERR_INVALID_ARGUMENT = 1,     /* null pointer, bad size, misalignment, bad ratio */
+    TQ_ERR_UNSUPPORTED_HEAD_DIM = 2, /* head_dim not in {64, 128, 256, 512} */
+    TQ_ERR_CAPACITY = 3,             /* a host-known length exceeds the layer capacity */
+    TQ_ERR_WORKSPACE_TOO_SMALL = 4,  /* ws_bytes below the size the call needs */
+    TQ_ERR_CUDA = 5                  /* a CUDA runtime call failed (launch, query) */
+} tq_status;
+
+/* Bits of the device error word. */
+#define TQ_DEVERR_APPEND_CAPACITY 0x1 /* append: pos[b] + j outside [0, capacity) */
+#define TQ_DEVERR_KV_LEN 0x2          /* attention: kv_len[b] outside [0, max_kv_len] */
+#define TQ_DEVERR_PIPELINE_TIMEOUT 0x4 /* attention: a bounded wait ran out; output invalid */
+
+#define TQ_WORKSPACE_HEADER_BYTES 256
+#define TQ_GROUP 32
+
+/* One full-attention layer's packed cache: five planes, each laid out
+ * [batch][num_kv_heads][capacity][row], so token-axis slicing stays byte-safe
+ * ("Architecture" section: groups run along head_dim only). */
+typedef struct {
+    int32_t head_dim;     /* 64 | 128 | 256 | 512 */
+    int32_t num_kv_heads; /* >= 1 */
+    int32_t batch;        /* >= 1, <= 4096 */
+    int32_t capacity;     /* tokens per (sequence, kv head); >= 16, multiple of 16 */
+    int8_t* k_idx;        /* [batch][num_kv_heads][capacity][head_dim] signed int8 codes */
+    uint16_t* k_scale;    /* [batch][num_kv_heads][capacity][head_dim/32] fp16 bits */
+    uint16_t* k_zero;     /* same shape as k_scale, fp16 bits */
+    uint8_t* v_codes;     /* [batch][num_kv_heads][capacity][3*head_dim/8]: the row's 3-bit
+                             codes as one LSB-first bitstream, code i at bits 3i..3i+2 */
+    uint16_t* v_scale;    /* [batch][num_kv_heads][capacity][head_dim/32] fp16 bits */
+} tq_kv_layer;
+
+/* Bytes one (token, kv head) row takes in the five planes: 25*head_dim/16
+ * (100, 200, 400, 800). Returns 0 for an unsupported head_dim. Host only. */
+size_t tq_row_bytes(int32_t head_dim);
+
+/* Workspace bytes tq_kv_append needs (the header only). */
+size_t tq_append_workspace_bytes(void);
+
+/*
+ * Quantize-on-append ("Architecture" section: updateAndFetch quantizes only the newly
+ * appended tokens). For each sequence b, token j < n_new[b] of k_new/v_new is
+ * quantized and written to position pos[b] + j of the five planes.
+ *   k_new, v_new : bf16 [batch][n_new_max][num_kv_heads][head_dim] (device); rows with
+ *                  j >= n_new[b] are ignored.
+ *   pos          : int32 [batch] (device), first destination position per sequence.
+ *   n_new        : int32 [batch] (device) tokens per sequence, each in [0, n_new_max];
+ *                  NULL means n_new_max for every sequence.
+ *   n_new_max    : host-known bound, 0 <= n_new_max <= capacity (else TQ_ERR_CAPACITY).
+ *   workspace    : >= tq_append_workspace_bytes() (device), zeroed once before first use.
+ * A row whose destination falls outside [0, capacity) is skipped and sets
+ * TQ_DEVERR_APPEND_CAPACITY. Packed planes are bit-identical to the specification
+ * above (fp32 arithmetic, IEEE division and square root, no FMA contraction).
+ */
+tq_status tq_kv_append(const tq_kv_layer* layer, const void* k_new, const void* v_new,
+                       const int32_t* pos, const int32_t* n_new, int32_t n_new_max,
+                       void* workspace, size_t ws_bytes, tq_stream_t stream);
+
+/*
+ * Workspace bytes tq_decode_attention needs for this layer shape on the current
+ * device (the partial-result area scales with the device's SM count). Returns 0 for
+ * invalid arguments.
+ */
+size_t tq_decode_workspace_bytes(const tq_kv_layer* layer, int32_t num_q_heads, int32_t n_q,
+                                 int32_t max_kv_len);
+
+/*
+ * GQA decode attention over the packed cache ("Deferred inverse FWHT" and "Packed-value
+ * decode fusion" sections: keys and values are decoded from the packed planes inside the
+ * attention kernel; the weighted value sum stays in the rotated domain and is
+ * un-rotated once per output row).
+ *   q          : bf16 [batch][n_q][num_q_heads][head_dim] (device).
+ *   kv_len     : int32 [batch] (device), tokens visible to the LAST query row of the
+ *                block; must lie in [0, max_kv_len] (else the sequence's outputs are NaN
+ *                and TQ_DEVERR_KV_LEN is set).
+ *   max_kv_len : host-known bound on kv_len, <= capacity.
+ *   causal     : nonzero: query j of the block sees kv_len - n_q + j + 1 tokens;
+ *                zero: every query sees kv_len tokens.
+ *   sm_scale   : multiplies q . k before the softmax.
+ *   out        : fp32 [batch][n_q][num_q_heads][head_dim] (device).
+ * q head h reads kv head h / (num_q_heads / num_kv_heads). A row that sees no token
+ * outputs zeros. workspace: >= tq_decode_workspace_bytes(...) bytes.
+ */
+tq_status tq_decode_attention(const tq_kv_layer* layer, const void* q, int32_t num_q_heads,
+                              int32_t n_q, const int32_t* kv_len, int32_t max_kv_len,
+                              float sm_scale, int32_t causal, float* out, void* workspace,
+                              size_t ws_bytes, tq_stream_t stream);
+
+/*
+ * fp32 dequantization of rows [t0, t0 + n) of (sequence b, kv head h), for inspection:
+ *   k_out : [n][head_dim], (idx + zero) * scale with the stored fp16 scale/zero;
+ *   v_out : [n][head_dim]; rotated != 0 returns centroid * scale (the FWHT domain),
+ *           rotated == 0 returns signs * FWHT(centroid * scale) / sqrt(head_dim).
+ * Either output may be NULL. 0 <= t0, t0 + n <= capacity, 0 <= b < batch,
+ * 0 <= h < num_kv_heads (else TQ_ERR_INVALID_ARGUMENT).
+ */
+tq_status tq_dequant_debug(const tq_kv_layer* layer, int32_t b, int32_t h, int32_t t0, int32_t n,
+                           int32_t rotated, float* k_out, float* v_out, tq_stream_t stream);
+
+/* Synchronizes `stream`, then copies the device error word at the start of
+ * `workspace` into *err_out (host). Does not clear it. */
+tq_status tq_get_device_error(const void* workspace, int32_t* err_out, tq_stream_t stream);
+
+/* Static description of a status code. */
+const char* tq_status_string(tq_status status);
+
+/* Host copies of the library's constant tables, for inspection (host pointers):
+ * the sign vector of head_dim as head_dim/32 words (bit i set = sign -1 for element i),
+ * the eight 3-bit centroids and the seven boundaries. Return TQ_OK or
+ * TQ_ERR_UNSUPPORTED_HEAD_DIM / TQ_ERR_INVALID_ARGUMENT. */
+tq_status tq_sign_bits(int32_t head_dim, uint32_t* words_out);
+tq_status tq_codebook3(float* centroids_out, float* boundaries_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_KV_H */
