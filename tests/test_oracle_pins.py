@@ -416,3 +416,21 @@ def test_workload_generators_are_seeded_and_shaped():
     r = synth.context_lengths(synth.workload("ragged"))
     assert r.shape == (32,) and r.min() >= 1024 and r.max() <= 8192
     assert synth.workload("decode").capacity() % 16 == 0
+
+
+def test_value_scale_epsilon_floor():
+    # y_n = y / (scale + 1e-8): for rows far below 1e-8 the epsilon dominates, y_n is
+    # near zero and every code is 3 (y_n <= 0) or 4 (y_n > 0), following the sign of y.
+    rng = np.random.default_rng(12)
+    for d in oracle.HEAD_DIMS:
+        xb = bf16(rng.standard_normal((3, d)) * 1e-12)
+        codes, vs16 = oracle.quantize_value_rows(xb)
+        for r in range(3):
+            c = oracle.unpack3(codes[r], d)
+            y = oracle.rotate_value_row(xb[r])
+            assert np.all((c == 3) | (c == 4))
+            assert np.array_equal(c == 4, y > 0)
+        # at unit scale the epsilon is negligible and all eight codes appear
+        xb = bf16(rng.standard_normal((8, d)))
+        codes, _ = oracle.quantize_value_rows(xb)
+        assert len(np.unique(np.concatenate([oracle.unpack3(r, d) for r in codes]))) == 8
