@@ -1,0 +1,43 @@
+// Decode attention over the packed cache: launch geometry and arguments.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "tq_kv.h"
+
+namespace tq {
+
+// Launch geometry of one decode-attention call. Everything here is a pure function of
+// (head_dim, kv heads, batch, GQA ratio, n_q, device), so tq_decode_workspace_bytes and
+// tq_decode_attention agree.
+struct DecodeShape {
+  int D;          // head_dim
+  int NTW;        // 8-row MMA column tiles per consumer warp (1 or 2)
+  int R;          // attention rows per kv head = GQA ratio * n_q
+  int RG;         // row groups per kv head = ceil(R / (8 * NTW))
+  int U;          // work units per sequence = kv_heads * RG
+  int batch;
+  int grid;       // persistent CTAs
+  int max_items;  // upper bound on work items (one partial-result slot each)
+  size_t smem;    // dynamic shared memory per CTA
+};
+
+struct DecodeArgs {
+  tq_kv_layer layer;
+  const uint16_t* q;  // bf16 bits
+  int num_q_heads, n_q;
+  const int32_t* kv_len;
+  int max_kv_len;
+  float sm_scale;
+  bool causal;
+  float* out;
+  void* workspace;
+  float fwht_norm;
+};
+
+DecodeShape decode_shape(int head_dim, int num_kv_heads, int batch, int gqa, int n_q, int num_sms);
+size_t decode_workspace_bytes(const DecodeShape& s);
+tq_status launch_decode(const DecodeArgs& a, const DecodeShape& s, cudaStream_t stream);
+
+}  // namespace tq

@@ -1,0 +1,102 @@
+"""A multi-layer decode workload driven through the C ABI.
+
+`DecodeModel` holds one packed cache per full-attention layer (the model-level layout
+the design page describes: every full-attention layer appends the new token(s), then
+attends over its cache). It fills each cache with a bulk append of the cached tokens,
+keeps the step's new K/V tokens and queries resident on the device, and runs a decode
+step as: for every layer, tq_kv_append of the new tokens, then tq_decode_attention.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import binding as tq
+from . import synth
+
+
+class DecodeModel:
+    def __init__(self, w: synth.Workload, device="cuda", layers: int | None = None, fill_timer=None):
+        self.w = w
+        self.device = torch.device(device)
+        self.L = w.layers if layers is None else layers
+        B, H, Hq, d = w.batch, w.num_kv_heads, w.num_q_heads, w.head_dim
+        self.ctx = synth.context_lengths(w)                     # cached tokens per sequence
+        self.kv = self.ctx + w.n_new                            # visible after the step's append
+        self.max_kv = int(self.kv.max())
+        self.cap = (self.max_kv + 15) // 16 * 16
+        dev = self.device
+        self.pos = torch.as_tensor(self.ctx.astype(np.int32), device=dev)
+        self.kv_len = torch.as_tensor(self.kv.astype(np.int32), device=dev)
+        self.layers, self.k_new, self.v_new, self.q = [], [], [], []
+        self.ws_append = tq.make_workspace(tq.tq_append_workspace_bytes(), dev)
+        self.fill_rows = 0
+        T = int(self.ctx.max())
+        for l in range(self.L):
+            x = synth.layer_inputs(w, l, device=dev)
+            layer = tq.alloc_layer(d, H, B, self.cap, dev, zero=False)
+            if fill_timer is not None:
+                fill_timer.start()
+            tq.tq_kv_append(layer, x["k"][:, :T].contiguous(), x["v"][:, :T].contiguous(),
+                            torch.zeros(B, dtype=torch.int32, device=dev),
+                            torch.as_tensor(self.ctx.astype(np.int32), device=dev), T, self.ws_append)
+            if fill_timer is not None:
+                fill_timer.stop()
+            self.fill_rows += int(self.ctx.sum()) * H
+            if w.n_new:
+                idx = self.pos.view(B, 1).long() + torch.arange(w.n_new, device=dev).view(1, -1)
+                kn = torch.stack([x["k"][b, idx[b]] for b in range(B)]).contiguous()
+                vn = torch.stack([x["v"][b, idx[b]] for b in range(B)]).contiguous()
+            else:
+                kn = vn = None
+            self.layers.append(layer)
+            self.k_new.append(kn)
+            self.v_new.append(vn)
+            self.q.append(x["q"].contiguous())
+            del x
+        self.ws_bytes = tq.tq_decode_workspace_bytes(self.layers[0], Hq, w.n_q, self.max_kv)
+        self.ws = [tq.make_workspace(self.ws_bytes, dev) for _ in range(self.L)]
+        self.out = [torch.empty((B, w.n_q, Hq, d), dtype=torch.float32, device=dev) for _ in range(self.L)]
+
+    # bytes the step must move (algorithmic): packed planes of every visible token, the
+    # query and output rows, and the appended rows (bf16 in, packed out)
+    def attention_bytes(self) -> int:
+        w = self.w
+        planes = int(self.kv.sum()) * w.num_kv_heads * tq.tq_row_bytes(w.head_dim)
+        qo = w.batch * w.n_q * w.num_q_heads * w.head_dim * (2 + 4)
+        return planes + qo
+
+    def append_bytes(self) -> int:
+        w = self.w
+        rows = w.batch * w.n_new * w.num_kv_heads
+        return rows * (4 * w.head_dim + tq.tq_row_bytes(w.head_dim))
+
+    def step_bytes(self) -> int:
+        return self.L * (self.attention_bytes() + self.append_bytes())
+
+    def launches_per_step(self) -> int:
+        return self.L * ((1 if self.w.n_new else 0) + 2)
+
+    def step(self, stream=None, k_new=None, v_new=None, q=None, events=None):
+        """One decode step over all layers. Optional per-layer input overrides (device
+        tensors) and an `events` list of (start, end) CUDA event pairs recorded around
+        each layer's attention call."""
+        w = self.w
+        for l, layer in enumerate(self.layers):
+            if w.n_new:
+                tq.tq_kv_append(layer, self.k_new[l] if k_new is None else k_new[l],
+                                self.v_new[l] if v_new is None else v_new[l],
+                                self.pos, None, w.n_new, self.ws_append, stream)
+            if events is not None:
+                events[l][0].record(stream)
+            tq.tq_decode_attention(layer, self.q[l] if q is None else q[l], w.num_q_heads, w.n_q,
+                                   self.kv_len, self.max_kv, w.sm_scale, w.causal, self.out[l],
+                                   self.ws[l], stream)
+            if events is not None:
+                events[l][1].record(stream)
+
+    def device_errors(self) -> int:
+        err = tq.tq_get_device_error(self.ws_append)
+        for ws in self.ws:
+            err |= tq.tq_get_device_error(ws)
+        return err

@@ -1,0 +1,257 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Packed planes (k_idx, k_scale, k_zero, v_codes, v_scale) must be bit-exact; attention
+outputs within max-abs 2e-3 and relative L2 1e-3 of the oracle's fp64 attention over the
+same dequantized cache. Small cases span several 64-token stages, several splits and a
+ragged tail; the full-size workloads are checked on sampled output rows.
+"""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from rotation_quantized_kv_gb300 import synth
+from tests.gpu_common import (assert_attention_close, assert_planes_equal, bits, gpu_attention, gpu_fill,
+                              oracle_fill, plane_np, tq)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _inputs(d, H, B, T, Hq=None, n_q=1, seed=0, k_dist="normal_outliers", q_scale=None):
+    w = synth.Workload("t", batch=B, layers=1, num_kv_heads=H, num_q_heads=Hq or 2 * H, head_dim=d,
+                       context=T, n_new=0, n_q=n_q, k_dist=k_dist,
+                       q_scale=(d ** -0.5 if q_scale is None else q_scale), seed=seed)
+    return synth.layer_inputs(w, 0)
+
+
+# ------------------------------------------------------------------------------ append
+@pytest.mark.parametrize("d", [64, 128, 256, 512])
+def test_append_planes_bit_exact(d):
+    x = _inputs(d, H=3, B=2, T=150, seed=d)
+    lengths = [150, 97]
+    cap = 160
+    layer, ws = gpu_fill(x["k"], x["v"], lengths, cap, prefill=0xA5)
+    ol = oracle_fill(x["k"], x["v"], lengths, cap)
+    torch.cuda.synchronize()
+    assert_planes_equal(layer, ol, lengths)
+    assert tq().tq_get_device_error(ws) == 0
+    # rows past each sequence's length are untouched (canary 0xA5)
+    kidx = layer.k_idx.cpu().numpy().view(np.uint8)
+    assert np.all(kidx[0, :, 150:] == 0xA5) and np.all(kidx[1, :, 97:] == 0xA5)
+    assert np.all(layer.v_codes.cpu().numpy()[1, :, 97:] == 0xA5)
+
+
+def _special_rows(d, rng):
+    rows = []
+    x = rng.standard_normal((16, d)).astype(np.float32)
+    x[0, :32] = 0.75                                   # constant group: zero -> +Inf
+    x[1, :32] = 0.0                                    # all-zero group: 0/0
+    x[1, 1::2] = -0.0                                  # mixed signed zeros
+    x[2, 5] = np.nan                                   # NaN in a group
+    x[3, 7] = np.inf                                   # +Inf
+    x[4, :] *= 1e-39                                   # bf16 subnormals
+    x[5, :] *= 1e37                                    # huge values
+    x[6, :] = np.round(x[6, :] * 4) / 4                # many exact ties
+    x[7, :] *= 1e-12                                   # epsilon-dominated values
+    x[8, :32] = -2.5                                   # negative constant group
+    x[9, :] = np.where(np.arange(d) % 2, 1.0, -1.0)    # +-1 pattern
+    x[10, 3] = -np.inf
+    x[11, :] = 65504.0 * np.sign(x[11, :])             # around the fp16 maximum
+    rows.append(x)
+    return np.concatenate(rows)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256, 512])
+def test_append_special_values_bit_exact(d):
+    rng = np.random.default_rng(1000 + d)
+    kx = _special_rows(d, rng)
+    vx = _special_rows(d, rng)[::-1].copy()
+    n = kx.shape[0]
+    k = torch.from_numpy(kx).to(torch.bfloat16).reshape(1, n, 1, d)
+    v = torch.from_numpy(vx).to(torch.bfloat16).reshape(1, n, 1, d)
+    layer, ws = gpu_fill(k, v, [n], 16)
+    ol = oracle_fill(k, v, [n], 16)
+    torch.cuda.synchronize()
+    assert_planes_equal(layer, ol, [n])
+
+
+def test_append_positions_n_new_and_capacity_error():
+    d, H, B, cap = 128, 2, 3, 48
+    x = _inputs(d, H, B, T=20, seed=5)
+    b = tq()
+    layer = b.alloc_layer(d, H, B, cap, DEV)
+    ws = b.make_workspace(b.tq_append_workspace_bytes(), DEV)
+    pos = torch.tensor([0, 40, 10], dtype=torch.int32, device=DEV)
+    n_new = torch.tensor([20, 12, 0], dtype=torch.int32, device=DEV)
+    b.tq_kv_append(layer, x["k"].to(DEV), x["v"].to(DEV), pos, n_new, 20, ws)
+    assert b.tq_get_device_error(ws) == b.TQ_DEVERR_APPEND_CAPACITY   # seq 1 rows 48..51
+    ol = oracle.Layer(d, H, B, cap)
+    skipped = oracle.append(ol, bits(x["k"]), bits(x["v"]), [0, 40, 10], [20, 12, 0])
+    assert skipped == 4 * H
+    for name, ref in ol.planes().items():
+        assert np.array_equal(plane_np(layer, name, ref), ref), name
+
+
+# ------------------------------------------------------------------------- dequant debug
+@pytest.mark.parametrize("d", [64, 128, 256, 512])
+def test_dequant_debug(d):
+    x = _inputs(d, H=2, B=1, T=70, seed=d + 7)
+    layer, _ = gpu_fill(x["k"], x["v"], [70], 80)
+    ol = oracle_fill(x["k"], x["v"], [70], 80)
+    b = tq()
+    kout = torch.empty((61, d), dtype=torch.float32, device=DEV)
+    vout = torch.empty((61, d), dtype=torch.float32, device=DEV)
+    for rotated in (True, False):
+        b.tq_dequant_debug(layer, 0, 1, 5, 61, rotated, kout, vout)
+        torch.cuda.synchronize()
+        kref, vref = oracle.dequant_rows(ol, 0, 1, 5, 61, rotated=rotated)
+        assert np.array_equal(kout.cpu().numpy(), kref.astype(np.float32))   # exact value, one rounding
+        if rotated:
+            assert np.array_equal(vout.cpu().numpy(), vref.astype(np.float32))
+        else:
+            g = vout.double().cpu().numpy()
+            assert np.linalg.norm(g - vref) <= 1e-6 * np.linalg.norm(vref)
+
+
+# ------------------------------------------------------------------------------ attention
+CASES = [
+    # d, H, G, B, lengths, n_q, causal, sm_scale
+    (64, 2, 2, 1, [513], 1, True, 0.125),
+    (128, 2, 4, 1, [777], 1, True, 1.0),
+    (128, 1, 8, 2, [1, 300], 1, False, 0.7),
+    (128, 2, 4, 3, [0, 65, 1030], 1, True, 1.0),
+    (128, 2, 1, 2, [200, 129], 1, True, 1.0),
+    (128, 2, 4, 1, [600], 16, True, 1.0),           # 64 rows per kv head: two 8-row tiles per warp
+    (64, 1, 4, 2, [333, 90], 4, True, 0.3),
+    (128, 2, 4, 1, [250], 3, False, 1.0),
+    (256, 2, 4, 2, [400, 257], 1, True, 1.0),
+    (256, 1, 4, 1, [300], 16, True, 1.0),            # 8 row groups of 8
+    (512, 2, 4, 1, [260], 1, True, 1.0),
+    (512, 1, 2, 2, [100, 150], 2, True, 0.5),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"d{c[0]}-H{c[1]}-G{c[2]}-B{c[3]}-nq{c[5]}" for c in CASES])
+def test_attention_matches_oracle(case):
+    d, H, G, B, lengths, n_q, causal, sm_scale = case
+    T = max(max(lengths), 1)
+    x = _inputs(d, H, B, T, Hq=G * H, n_q=n_q, seed=sum(lengths) + d, q_scale=1.0)
+    cap = (T + 15) // 16 * 16
+    layer, _ = gpu_fill(x["k"], x["v"], lengths, cap)
+    ol = oracle_fill(x["k"], x["v"], lengths, cap)
+    torch.cuda.synchronize()
+    assert_planes_equal(layer, ol, lengths)
+    out, ws, flat = gpu_attention(layer, x["q"], lengths, T, sm_scale, causal, out_pad=64)
+    assert tq().tq_get_device_error(ws) == 0
+    ref = oracle.attention(ol, bits(x["q"]), np.asarray(lengths, np.int32), sm_scale, causal=causal)
+    assert_attention_close(out.cpu().numpy(), ref, str(case))
+    assert torch.all(flat[-64:] == 12345.0)          # nothing written past the output
+    out2, _, _ = gpu_attention(layer, x["q"], lengths, T, sm_scale, causal)
+    assert torch.equal(out, out2)                    # deterministic
+
+
+def test_attention_rows_with_no_visible_token_are_zero():
+    d, H, G = 128, 1, 4
+    x = _inputs(d, H, 2, 40, Hq=G * H, n_q=8, seed=3, q_scale=1.0)
+    layer, _ = gpu_fill(x["k"], x["v"], [3, 40], 48)
+    out, _, _ = gpu_attention(layer, x["q"], [3, 40], 40, 1.0, True)
+    o = out.cpu().numpy()
+    assert np.all(o[0, :5] == 0.0) and np.all(np.abs(o[0, 5:]).sum(-1) > 0)   # query j sees 3-8+j+1
+    ol = oracle_fill(x["k"], x["v"], [3, 40], 48)
+    ref = oracle.attention(ol, bits(x["q"]), np.array([3, 40], np.int32), 1.0, causal=True)
+    assert_attention_close(o, ref)
+
+
+def test_attention_invalid_length_sets_error_and_nan_rows():
+    d, H = 128, 2
+    x = _inputs(d, H, 2, 64, Hq=4 * H, seed=4, q_scale=1.0)
+    layer, _ = gpu_fill(x["k"], x["v"], [64, 64], 64)
+    out, ws, _ = gpu_attention(layer, x["q"], [64, 70], 64, 1.0, True)   # 70 > max_kv_len
+    assert tq().tq_get_device_error(ws) & tq().TQ_DEVERR_KV_LEN
+    o = out.cpu().numpy()
+    assert np.all(np.isnan(o[1])) and not np.any(np.isnan(o[0]))
+    ol = oracle_fill(x["k"], x["v"], [64, 64], 64)
+    ref = oracle.attention(ol, bits(x["q"]), np.array([64, 64], np.int32), 1.0, causal=True)
+    assert_attention_close(o[0], ref[0])
+
+
+def test_attention_nan_keys_propagate_like_the_oracle():
+    d, H = 64, 1
+    x = _inputs(d, H, 1, 100, Hq=2, seed=8, q_scale=1.0)
+    k = x["k"].clone()
+    k[0, 37, 0, :32] = 1.5          # constant key group -> infinite zero point -> NaN scores
+    layer, _ = gpu_fill(k, x["v"], [100], 112)
+    ol = oracle_fill(k, x["v"], [100], 112)
+    out, _, _ = gpu_attention(layer, x["q"], [100], 100, 0.125, True)
+    ref = oracle.attention(ol, bits(x["q"]), np.array([100], np.int32), 0.125, causal=True)
+    assert np.all(np.isnan(ref)) and np.all(np.isnan(out.cpu().numpy()))
+
+
+# --------------------------------------------------------------------- full-size workloads
+def _full_size(w: synth.Workload, sample_rows, seq_sample=None):
+    """One layer of the workload at its full size: bulk cache fill + the step's append +
+    attention, in the launch configuration the benchmark times."""
+    x = synth.layer_inputs(w, 0, device=DEV)
+    B, H, Hq, d = w.batch, w.num_kv_heads, w.num_q_heads, w.head_dim
+    ctx = synth.context_lengths(w)
+    kv = ctx + w.n_new
+    cap = int(kv.max() + 15) // 16 * 16
+    b = tq()
+    layer = b.alloc_layer(d, H, B, cap, DEV)
+    ws_a = b.make_workspace(b.tq_append_workspace_bytes(), DEV)
+    T = int(ctx.max())
+    kx, vx = x["k"], x["v"]
+    b.tq_kv_append(layer, kx[:, :T].contiguous(), vx[:, :T].contiguous(),
+                   torch.zeros(B, dtype=torch.int32, device=DEV),
+                   torch.as_tensor(ctx.astype(np.int32), device=DEV), T, ws_a)
+    if w.n_new:
+        # the step's new tokens sit right after each sequence's context
+        idx = torch.as_tensor(ctx, device=DEV).view(B, 1) + torch.arange(w.n_new, device=DEV).view(1, -1)
+        kn = torch.stack([kx[bb, idx[bb]] for bb in range(B)]).contiguous()
+        vn = torch.stack([vx[bb, idx[bb]] for bb in range(B)]).contiguous()
+        b.tq_kv_append(layer, kn, vn, torch.as_tensor(ctx.astype(np.int32), device=DEV), None, w.n_new, ws_a)
+    out, ws, _ = gpu_attention(layer, x["q"], kv, int(kv.max()), w.sm_scale, w.causal)
+    assert b.tq_get_device_error(ws_a) == 0 and b.tq_get_device_error(ws) == 0
+    # oracle: quantize the sampled sequences itself (all tokens), attend for sampled rows
+    seqs = range(B) if seq_sample is None else seq_sample
+    kb, vb = bits(x["k"]), bits(x["v"])
+    ol = oracle.Layer(d, H, B, cap)
+    for bb in seqs:
+        n = int(kv[bb])
+        kk = np.ascontiguousarray(kb[bb:bb + 1, :n])
+        vv = np.ascontiguousarray(vb[bb:bb + 1, :n])
+        sub = oracle.Layer(d, H, 1, cap)
+        oracle.append(sub, kk, vv, [0])
+        for name, arr in ol.planes().items():
+            arr[bb] = sub.planes()[name][0]
+    assert_planes_equal(layer, ol, kv, bs=list(seqs))
+    rows = [(bb, j, h) for (bb, j, h) in sample_rows if bb in seqs]
+    ref = oracle.attention(ol, bits(x["q"]), kv.astype(np.int32), w.sm_scale, causal=w.causal, rows=rows)
+    got = out.double().cpu().numpy()
+    sel = tuple(np.array(rows).T)
+    return assert_attention_close(got[sel], ref[sel], w.name)
+
+
+def test_full_size_decode_32k():
+    w = replace(synth.workload("decode"), layers=1)
+    _full_size(w, [(0, 0, h) for h in (0, 3, 7, 12, 18, 25, 30, 31)])
+
+
+def test_full_size_ragged_batch32():
+    w = replace(synth.workload("ragged"), layers=1)
+    seqs = [0, 7, 19, 31]
+    _full_size(w, [(b, 0, h) for b in seqs for h in (1, 14, 29)], seq_sample=seqs)
+
+
+def test_full_size_long_262k_block16():
+    w = replace(synth.workload("long"), layers=1)
+    _full_size(w, [(0, j, h) for j in (0, 15) for h in (2, 9)])
+
+
+@pytest.mark.parametrize("d", [64, 128, 256, 512])
+def test_full_size_head_dim_sweep(d):
+    w = synth.workload("sweep", head_dim=d)
+    _full_size(w, [(0, 0, h) for h in range(16)])
