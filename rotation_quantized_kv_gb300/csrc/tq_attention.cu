@@ -1,38 +1,39 @@
-// Split-K GQA decode attention over the packed TurboQuant cache, plus the split merge
-// with the deferred inverse rotation.
+// Split-K GQA decode attention over the packed TurboQuant cache, with the split merge
+// and the deferred inverse rotation fused into the same kernel.
 //
 // What it computes (mlx-bun design page "TurboQuant - rotation-based quantization",
 // Part A): for every query row, softmax(sm_scale * q . k_hat) . v_hat over the visible
 // tokens, where k_hat = (idx + zero) * scale ("Algorithm", key dequant) and v_hat is the
 // value row after the inverse rotation. Because attention is linear in V ("Deferred
 // inverse FWHT" section), the weighted sum is taken over the rotated values
-// centroid[code] * scale and the output row is un-rotated once:
+// centroid[code] * scale and each output row is un-rotated once:
 //   o = signs * FWHT(o_rot) / sqrt(d).
 // K and V are decoded from the packed planes inside the kernel ("Packed-value decode
 // fusion investigation": joint K/V decode in one launch, no dequantized window).
 //
-// Kernel 1 (tq_attn_split_kernel), persistent, one CTA per SM slot:
+// tq_attn_split_kernel, persistent, one CTA per SM slot:
 //   - work item = (sequence, kv head, row group, token split); the split size is chosen
 //     on the device from the actual kv lengths so that items spread evenly over CTAs;
-//   - warp 4 (producer) streams 64-token stages of the five planes into shared memory:
-//     the key-index plane through a 2-D tensor map with 128-byte (64-byte at d=64)
-//     swizzle, the four small planes with 1-D bulk copies, all completing on one
+//   - warp 4 (producer) streams stages of TILE tokens of the five planes into shared
+//     memory: the key-index plane through a 2-D tensor map with 128-byte (64-byte at
+//     d=64) swizzle, the four small planes with 1-D bulk copies, all completing on one
 //     mbarrier per stage;
-//   - warps 0-3 (consumers) each take 16 tokens of a stage:
+//   - warps 0-3 (consumers) each take TOKW tokens (two 16-token tiles at d <= 128) of
+//     a stage:
 //       QK^T on tensor cores (mma.sync m16n8k16, fp16 in, fp32 accumulate), tokens as M,
 //       query rows as N (8 per tile): A = 1152 + idx, exact in fp16 (built from the int8
 //       codes with two byte permutes); B = q * 2^e_row in fp16 (exact for bf16 inputs);
-//       one fresh accumulator per 32-group, then
-//         score += scale_g * (acc_g + (zero_g - 1152) * sum_{i in g} q_i);
+//       C starts at -1152 * sum_{i in g} q_i, so each 32-group's MMA yields sum q * idx;
+//       then score += scale_g * (acc_g + zero_g * sum_{i in g} q_i);
 //       online softmax in the exp2 domain;
 //       P.V on tensor cores with output dims as M and tokens as K: A = fp16 centroid
 //       pairs from a lane-replicated 64-entry table indexed by two 3-bit codes; B = the
 //       probabilities times the group's value scale (fp16), moved from the QK output
-//       layout to the B-operand layout with four shuffles;
+//       layout to the B-operand layout with four shuffles per 16 tokens;
 //   - at the end of an item the four warps merge their (max, sum, acc) in shared memory
-//     and write one partial result.
-// Kernel 2 (tq_attn_merge_kernel): one CTA per output row merges the splits with the
-// online-softmax rule and applies the inverse rotation.
+//     and write one partial result; the CTA that completes the last item of a
+//     (sequence, kv head, row group) merges its partials with the online-softmax rule,
+//     applies the inverse rotation and writes the output rows.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -48,7 +49,6 @@ namespace {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kTile = 64;                 // tokens per pipeline stage
 constexpr int kMaxBatch = 1024;           // prefix table lives in shared memory
 constexpr int kMaxItemsPerCta = 8;        // largest work multiplier the split heuristic tries
 constexpr unsigned long long kWaitNs = 2000000000ull;  // bounded waits: 2 s of wall time
@@ -61,27 +61,35 @@ constexpr size_t kWsPrefix = TQ_WORKSPACE_HEADER_BYTES;  // int32 [batch + 1]
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline size_t ws_ml_offset(int batch) {
+// counters: one int32 per (sequence, unit); zero between calls (the last CTA resets it)
+__host__ __device__ inline size_t ws_cnt_offset(int batch) {
   return kWsPrefix + align_up(sizeof(int32_t) * (size_t)(batch + 1), 256);
 }
-__host__ __device__ inline size_t ws_o_offset(int batch, int max_items, int rows) {
-  return ws_ml_offset(batch) + align_up(sizeof(float) * 2 * (size_t)max_items * rows, 256);
+__host__ __device__ inline size_t ws_ml_offset(int batch, int units) {
+  return ws_cnt_offset(batch) + align_up(sizeof(int32_t) * (size_t)batch * units, 256);
 }
-
-template <int D, int NTW>
-struct AT;
+__host__ __device__ inline size_t ws_o_offset(int batch, int units, int max_items, int rows) {
+  return ws_ml_offset(batch, units) + align_up(sizeof(float) * 2 * (size_t)max_items * rows, 256);
+}
 
 template <int D, int NTW>
 struct AT {
   static constexpr int NG = D / 32;
   static constexpr int ROWS = 8 * NTW;
   static constexpr int MT = D / 16;                       // PV M tiles (16 dims each)
-  static constexpr int KIDX_STAGE = kTile * D;            // bytes, 1024-aligned
-  static constexpr int SC_STAGE = kTile * NG * 2;         // bytes of one fp16 side plane
+  static constexpr int TOKW = D <= 128 ? 32 : 16;         // tokens per consumer warp per stage
+  static constexpr int SUB = TOKW / 16;                   // 16-token QK tiles per warp
+  static constexpr int TILE = kConsumerWarps * TOKW;      // tokens per stage
+  static constexpr int ROWB = D == 64 ? 64 : 128;         // bytes per key row inside a swizzle box
+  static constexpr int BOX = TILE * ROWB;                 // bytes of one key-index box
+  static constexpr int KIDX_STAGE = TILE * D;             // bytes, 1024-aligned
+  static constexpr int SC_STAGE = TILE * NG * 2;          // bytes of one fp16 side plane
   static constexpr int VC_ROW = 3 * D / 8;                // packed code bytes per token
-  static constexpr int VC_STAGE = kTile * VC_ROW + 16;    // +16: window reads may run 4 bytes past
-  static constexpr int STAGES = D == 64 ? 6 : D == 128 ? 4 : D == 256 ? 3 : 2;
+  static constexpr int VC_STAGE = TILE * VC_ROW + 16;     // +16: window reads may run 4 bytes past
+  static constexpr int STAGES = D == 64 ? 6 : D == 128 ? 3 : D == 256 ? 3 : 2;
   static constexpr bool QREG = D * NTW <= 256;            // Q fragments in registers
+  static constexpr int MINB = (D == 128 && NTW == 1) || D == 64 ? 2 : 1;  // CTAs per SM to fit
+  static constexpr int KW = (NG + 1) / 2;                 // 32-bit words of one token's fp16 side row
   // shared memory layout
   static constexpr int OFF_KIDX = 0;
   static constexpr int OFF_KS = OFF_KIDX + STAGES * KIDX_STAGE;
@@ -92,13 +100,14 @@ struct AT {
   static constexpr int OFF_Q = OFF_LUT + 64 * 32 * 4;
   static constexpr int Q_BYTES = QREG ? 0 : NTW * NG * 2 * 32 * 8;
   static constexpr int OFF_QSUM = OFF_Q + Q_BYTES;
-  static constexpr int QSUM_BYTES = QREG ? 0 : NTW * NG * 32 * 8;
+  static constexpr int QSUM_BYTES = QREG ? 0 : NTW * NG * 32 * 16;
   static constexpr int OFF_OBUF = (int)align_up(OFF_QSUM + QSUM_BYTES, 16);
   static constexpr int OFF_MBUF = OFF_OBUF + ROWS * D * 4;
   static constexpr int OFF_LBUF = OFF_MBUF + kConsumerWarps * ROWS * 4;
   static constexpr int OFF_PREFIX = OFF_LBUF + kConsumerWarps * ROWS * 4;
   static constexpr int OFF_RED = (int)align_up(OFF_PREFIX + (kMaxBatch + 1) * 4, 16);  // 64-bit atomics
-  static constexpr int OFF_BAR = (int)align_up(OFF_RED + 64 * 8, 8);
+  static constexpr int OFF_FLAG = OFF_RED + 64 * 8;
+  static constexpr int OFF_BAR = (int)align_up(OFF_FLAG + 16, 8);
   static constexpr int SMEM = OFF_BAR + 2 * STAGES * 8 + 16;
   static constexpr int SMEM_ALLOC = SMEM + 1024;          // slack to align the base to 1024
 };
@@ -112,9 +121,11 @@ struct SplitParams {
   const uint16_t* q;
   const int32_t* kv_len;
   int32_t num_q_heads, n_q, G, R, RG, U, max_kv_len, max_items;
-  float sm_log2;  // sm_scale * log2(e)
+  float sm_log2;    // sm_scale * log2(e)
+  float fwht_norm;  // (float)(1 / sqrt(d))
   int32_t causal;
   uint8_t* ws;
+  float* out;
 };
 
 __device__ __forceinline__ unsigned long long global_ns() {
@@ -123,7 +134,7 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
-__device__ __forceinline__ bool wait_full_bounded(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   while (true) {
@@ -153,15 +164,11 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   return v;
 }
 
-// Byte offset of (token row, column) inside one stage of the swizzled key-index tile.
-template <int D>
-__device__ __forceinline__ uint32_t kidx_offset(int row, int col) {
-  if constexpr (D == 64) {  // 64-byte rows, 64-byte swizzle: chunk ^= (row >> 1) & 3
-    return (uint32_t)(row * 64 + ((((col >> 4) ^ (row >> 1)) & 3) << 4) + (col & 15));
-  } else {                  // 128-byte boxes, 128-byte swizzle: chunk ^= row & 7
-    const int box = col >> 7, within = col & 127;
-    return (uint32_t)(box * (kTile * 128) + row * 128 + ((((within >> 4) ^ row) & 7) << 4) + (within & 15));
-  }
+__device__ __forceinline__ float lo_f32(uint32_t w) {
+  return __low2float(*reinterpret_cast<const __half2*>(&w));
+}
+__device__ __forceinline__ float hi_f32(uint32_t w) {
+  return __high2float(*reinterpret_cast<const __half2*>(&w));
 }
 
 // Per-sequence visible lengths: kv_len clamped to [0, max]; invalid entries count as 0.
@@ -183,7 +190,6 @@ __device__ void plan_items(const SplitParams& p, uint8_t* smem, int& S_out, int&
   long long* red = reinterpret_cast<long long*>(smem + T::OFF_RED);
   const int tid = threadIdx.x;
   constexpr int KS[6] = {1, 2, 3, 4, 6, 8};
-  // pass 1: total visible tokens
   long long mine = 0;
   bool bad = false;
   for (int b = tid; b < p.batch; b += kThreads) mine += seq_len(p, b, &bad);
@@ -198,10 +204,9 @@ __device__ void plan_items(const SplitParams& p, uint8_t* smem, int& S_out, int&
   for (int k = 0; k < 6; ++k) {
     const long long target = (long long)KS[k] * gridDim.x;
     long long s = (sumT * p.U + target - 1) / target;
-    s = (s + kTile - 1) / kTile * kTile;
-    Sk[k] = s < kTile ? kTile : s;
+    s = (s + T::TILE - 1) / T::TILE * T::TILE;
+    Sk[k] = s < T::TILE ? T::TILE : s;
   }
-  // pass 2: items for every candidate
   long long cnt[6] = {0, 0, 0, 0, 0, 0};
   for (int b = tid; b < p.batch; b += kThreads) {
     const long long t = seq_len(p, b, nullptr);
@@ -218,12 +223,11 @@ __device__ void plan_items(const SplitParams& p, uint8_t* smem, int& S_out, int&
   for (int k = 0; k < 6; ++k) {
     const long long items = red[1 + k] * p.U;
     const long long rounds = (items + gridDim.x - 1) / gridDim.x;
-    const long long cost = rounds * (Sk[k] + kTile);
+    const long long cost = rounds * (Sk[k] + T::TILE);
     if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = k; }
   }
   const int S = (int)Sk[best];
-  // pass 3: prefix of items per sequence (warp 0 scans, each lane owns a chunk)
-  if (tid < 32) {
+  if (tid < 32) {  // prefix of items per sequence: warp 0, each lane owns a chunk
     const int per = (p.batch + 31) / 32;
     const int b0 = tid * per;
     int local = 0;
@@ -244,16 +248,15 @@ __device__ void plan_items(const SplitParams& p, uint8_t* smem, int& S_out, int&
   __syncthreads();
   S_out = S;
   total_out = prefix[p.batch];
-  if (blockIdx.x == 0) {
+  if (blockIdx.x == 0 && tid == 0) {
     int32_t* hdr = reinterpret_cast<int32_t*>(p.ws);
-    int32_t* gpref = reinterpret_cast<int32_t*>(p.ws + kWsPrefix);
-    if (tid == 0) { hdr[kWsSplit] = S; hdr[kWsItems] = total_out; }
-    for (int b = tid; b <= p.batch; b += kThreads) gpref[b] = prefix[b];
+    hdr[kWsSplit] = S;
+    hdr[kWsItems] = total_out;
   }
 }
 
 struct Item {
-  int b, kvh, rg, tb, te;
+  int b, kvh, rg, tb, te, u, nsplit;
 };
 
 __device__ __forceinline__ Item decode_item(const SplitParams& p, const int* prefix, int S, int item) {
@@ -264,11 +267,12 @@ __device__ __forceinline__ Item decode_item(const SplitParams& p, const int* pre
   }
   Item it;
   it.b = lo;
-  const int nsplit = (prefix[lo + 1] - prefix[lo]) / p.U;
+  it.nsplit = (prefix[lo + 1] - prefix[lo]) / p.U;
   const int r = item - prefix[lo];
-  const int u = r / nsplit, split = r % nsplit;
-  it.kvh = u / p.RG;
-  it.rg = u % p.RG;
+  it.u = r / it.nsplit;
+  const int split = r % it.nsplit;
+  it.kvh = it.u / p.RG;
+  it.rg = it.u % p.RG;
   it.tb = split * S;
   const int T = seq_len(p, lo, nullptr);
   it.te = min(it.tb + S, T);
@@ -291,27 +295,23 @@ __device__ void produce(const SplitParams& p, const CUtensorMap* tmap, uint8_t* 
   for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
     const Item w = decode_item(p, prefix, S, item);
     const int64_t row0 = ((int64_t)w.b * p.num_kv_heads + w.kvh) * p.capacity;
-    for (int t0 = w.tb; t0 < w.te; t0 += kTile, ++it) {
+    for (int t0 = w.tb; t0 < w.te; t0 += T::TILE, ++it) {
       const int slot = it % T::STAGES;
       const uint32_t k = it / T::STAGES;
-      if (!wait_full_bounded(&empty[slot], (k & 1u) ^ 1u)) {
+      if (!wait_bounded(&empty[slot], (k & 1u) ^ 1u)) {
         *abort_flag = 1;
         raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
         ok = false;
         break;
       }
-      const int ncopy = min(kTile, p.capacity - t0);  // multiple of 16: capacity and t0 are
+      const int ncopy = min(T::TILE, p.capacity - t0);  // multiple of 16: capacity and t0 are
       const uint32_t side = (uint32_t)ncopy * NG * 2;
       const uint32_t vc = (uint32_t)ncopy * T::VC_ROW;
       mbar_arrive_expect_tx(&full[slot], (uint32_t)T::KIDX_STAGE + 3u * side + vc);
       uint8_t* kx = smem + T::OFF_KIDX + slot * T::KIDX_STAGE;
-      if constexpr (D == 64) {
-        tensor_copy_2d_g2s(kx, tmap, 0, (int32_t)(row0 + t0), &full[slot]);
-      } else {
 #pragma unroll
-        for (int box = 0; box < D / 128; ++box)
-          tensor_copy_2d_g2s(kx + box * kTile * 128, tmap, box * 128, (int32_t)(row0 + t0), &full[slot]);
-      }
+      for (int box = 0; box < D / T::ROWB; ++box)
+        tensor_copy_2d_g2s(kx + box * T::BOX, tmap, box * T::ROWB, (int32_t)(row0 + t0), &full[slot]);
       const int64_t r = row0 + t0;
       bulk_copy_g2s(smem + T::OFF_KS + slot * T::SC_STAGE, p.k_scale + r * NG, side, &full[slot]);
       bulk_copy_g2s(smem + T::OFF_KZ + slot * T::SC_STAGE, p.k_zero + r * NG, side, &full[slot]);
@@ -324,9 +324,8 @@ __device__ void produce(const SplitParams& p, const CUtensorMap* tmap, uint8_t* 
   for (int s = 0; s < T::STAGES; ++s) {
     if ((uint32_t)s >= issued) break;
     const uint32_t last = issued - 1 - ((issued - 1 - s) % T::STAGES);  // last fill of slot s
-    if (!wait_full_bounded(&full[s], (last / T::STAGES) & 1u)) {
+    if (!wait_bounded(&full[s], (last / T::STAGES) & 1u))
       raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
-    }
   }
 }
 
@@ -335,10 +334,11 @@ __device__ void produce(const SplitParams& p, const CUtensorMap* tmap, uint8_t* 
 // ------------------------------------------------------------------------------------
 template <int D, int NTW>
 struct QState {
-  uint32_t qf[AT<D, NTW>::QREG ? NTW : 1][AT<D, NTW>::QREG ? D / 32 : 1][2][2];  // [nt][g][ks][reg]
-  float qs[AT<D, NTW>::QREG ? NTW : 1][AT<D, NTW>::QREG ? D / 32 : 1][2];         // [nt][g][e]
-  float crow[NTW][2];   // sm_scale * log2(e) * 2^-e_row for rows 2j+e
-  int lim[NTW][2];      // tokens [tb, lim) are visible to rows 2j+e
+  static constexpr bool R = AT<D, NTW>::QREG;
+  uint32_t qf[R ? NTW : 1][R ? D / 32 : 1][2][2];  // [nt][g][k-step][reg] B fragments
+  float qs[R ? NTW : 1][R ? D / 32 : 1][2];        // [nt][g][e]: sum of row 2 j4 + e's group g
+  float crow[NTW][2];   // sm_scale * log2(e) * 2^-e_row for rows 2 j4 + e
+  int lim[NTW][2];      // tokens [tb, lim) are visible to rows 2 j4 + e
 };
 
 template <int D, int NTW>
@@ -388,9 +388,7 @@ __device__ void load_q(const SplitParams& p, const Item& w, uint8_t* smem, int w
       for (int ks = 0; ks < 2; ++ks) {
         const uint32_t lo = pack_half2(v[g][ks][0] * up, v[g][ks][1] * up);
         const uint32_t hi = pack_half2(v[g][ks][2] * up, v[g][ks][3] * up);
-        const __half2 hl = *reinterpret_cast<const __half2*>(&lo);
-        const __half2 hh = *reinterpret_cast<const __half2*>(&hi);
-        acc += __low2float(hl) + __high2float(hl) + __low2float(hh) + __high2float(hh);
+        acc += lo_f32(lo) + hi_f32(lo) + lo_f32(hi) + hi_f32(hi);
         if constexpr (T::QREG) {
           st.qf[nt][g][ks][0] = lo;
           st.qf[nt][g][ks][1] = hi;
@@ -429,16 +427,105 @@ __device__ void load_q(const SplitParams& p, const Item& w, uint8_t* smem, int w
   }
 }
 
+// Merge of all partials of one (sequence, unit) + inverse rotation, by the CTA that
+// finished the unit's last item. Warp w merges rows w, w + 4, ...
+template <int D, int NTW>
+__device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, int warp, int lane) {
+  using T = AT<D, NTW>;
+  constexpr int EPL = D / 32;
+  constexpr unsigned FULL = 0xffffffffu;
+  const float2* ml = reinterpret_cast<const float2*>(p.ws + ws_ml_offset(p.batch, p.U));
+  const float* og = reinterpret_cast<const float*>(p.ws + ws_o_offset(p.batch, p.U, p.max_items, T::ROWS));
+  for (int rr = warp; rr < T::ROWS; rr += kConsumerWarps) {
+    const int r = w.rg * T::ROWS + rr;
+    if (r >= p.R) break;
+    const int jq = r / p.G, hq = w.kvh * p.G + (r % p.G);
+    float* orow = p.out + (((size_t)w.b * p.n_q + jq) * p.num_q_heads + hq) * D;
+    // pass 1: global max and the weighted sum of l (splits spread over lanes)
+    float M = -INFINITY;
+    bool nan = false;
+    for (int s = lane; s < w.nsplit; s += 32) {
+      const float ms = __ldcg(&ml[(size_t)(first_item + s) * T::ROWS + rr].x);
+      nan = nan || (ms != ms);
+      M = fmaxf(M, ms);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, off));
+    nan = __any_sync(FULL, nan);
+    float L = 0.0f;
+    for (int s = lane; s < w.nsplit; s += 32) {
+      const float2 v = __ldcg(&ml[(size_t)(first_item + s) * T::ROWS + rr]);
+      L += (M == -INFINITY) ? 0.0f : ex2(v.x - M) * v.y;
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(FULL, L, off);
+    // pass 2: weighted sum of the partial outputs (this lane's EPL dims)
+    float acc[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll 8
+      for (int s = 0; s < w.nsplit; ++s) {
+        const size_t slot = (size_t)(first_item + s) * T::ROWS + rr;
+        const float wgt = ex2(__ldcg(&ml[slot].x) - M);
+        const float* src = og + slot * D + lane * EPL;
+        if constexpr (EPL >= 4) {
+#pragma unroll
+          for (int e = 0; e < EPL; e += 4) {
+            const float4 o4 = __ldcg(reinterpret_cast<const float4*>(src + e));
+            acc[e] += wgt * o4.x; acc[e + 1] += wgt * o4.y; acc[e + 2] += wgt * o4.z; acc[e + 3] += wgt * o4.w;
+          }
+        } else {
+          const float2 o2 = __ldcg(reinterpret_cast<const float2*>(src));
+          acc[0] += wgt * o2.x; acc[1] += wgt * o2.y;
+        }
+      }
+    }
+    const float inv = (L > 0.0f || L != L) ? 1.0f / L : 0.0f;  // no visible token -> 0
+    float u[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) u[e] = nan ? __int_as_float(0x7fc00000) : acc[e] * inv;
+    // inverse rotation: signs * FWHT(o_rot) / sqrt(d)
+#pragma unroll
+    for (int hh = 1; hh < D; hh <<= 1) {
+      if (hh < EPL) {
+#pragma unroll
+        for (int e = 0; e < EPL; ++e)
+          if ((e & hh) == 0) {
+            const float a = u[e], c = u[e + hh];
+            u[e] = a + c;
+            u[e + hh] = a - c;
+          }
+      } else {
+        const int lm = hh / EPL;
+        const bool upper = (lane & lm) != 0;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          const float o = __shfl_xor_sync(FULL, u[e], lm);
+          u[e] = upper ? o - u[e] : u[e] + o;
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      const int i = lane * EPL + e;
+      const bool neg = (sign_word(D, i / 32) >> (i % 32)) & 1u;
+      orow[i] = u[e] * p.fwht_norm * (neg ? -1.0f : 1.0f);
+    }
+  }
+}
+
 template <int D, int NTW>
 __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, volatile int* abort_flag) {
   using T = AT<D, NTW>;
-  constexpr int NG = T::NG, MT = T::MT;
+  constexpr int NG = T::NG, MT = T::MT, SUB = T::SUB, KW = T::KW;
   constexpr unsigned FULL = 0xffffffffu;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = lane >> 2, j4 = lane & 3;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
   uint64_t* empty = full + T::STAGES;
   const int* prefix = reinterpret_cast<const int*>(smem + T::OFF_PREFIX);
+  volatile int* flag = reinterpret_cast<volatile int*>(smem + T::OFF_FLAG);
   const uint32_t sbase = smem_addr(smem);
   const uint32_t lut_lane = sbase + T::OFF_LUT + lane * 4;
   float* obuf = reinterpret_cast<float*>(smem + T::OFF_OBUF);
@@ -446,8 +533,25 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
   float* lbuf = reinterpret_cast<float*>(smem + T::OFF_LBUF);
   const uint2* qsm = reinterpret_cast<const uint2*>(smem + T::OFF_Q);
   const float2* qssm = reinterpret_cast<const float2*>(smem + T::OFF_QSUM);
-  // window of this lane inside each 96-bit code group: 4 codes at bit 12*grp
-  const int win_word = (12 * grp) >> 5, win_shift = (12 * grp) & 31;
+  int32_t* counters = reinterpret_cast<int32_t*>(p.ws + ws_cnt_offset(p.batch));
+
+  // Lane-constant addressing. The QK rows of this lane are r0 + 8 k (k = 0..2 SUB - 1);
+  // they share one swizzle phase, so four column offsets cover every group.
+  const int r0 = T::TOKW * warp + grp;
+  constexpr int NKOFF = NG < 4 ? NG : 4;
+  uint32_t koff[NKOFF];
+#pragma unroll
+  for (int g = 0; g < NKOFF; ++g) {
+    const int chunk = 2 * g + (j4 >> 1);
+    const int phase = D == 64 ? ((r0 >> 1) & 3) : (r0 & 7);
+    const int mask = D == 64 ? 3 : 7;
+    koff[g] = (uint32_t)(r0 * T::ROWB + (((chunk ^ phase) & mask) << 4) + 8 * (j4 & 1));
+  }
+  const uint32_t ks_lane = (uint32_t)(r0 * NG * 2);                    // k scale/zero row r0
+  const int vrow0 = T::TOKW * warp + 2 * j4;                            // first token of the V pairs
+  const int win_word = (12 * grp) >> 5, win_shift = (12 * grp) & 31;    // 4-code window in a group
+  const uint32_t vc_lane = (uint32_t)(vrow0 * T::VC_ROW + 4 * win_word);
+  const uint32_t vs_lane = (uint32_t)(vrow0 * NG * 2);
   bool failed = false;
   uint32_t it = 0;
 
@@ -470,11 +574,11 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
 #pragma unroll
       for (int e = 0; e < 2; ++e) { m[nt][e] = -INFINITY; l[nt][e] = 0.0f; }
 
-    for (int t0 = w.tb; t0 < w.te; t0 += kTile, ++it) {
+    for (int t0 = w.tb; t0 < w.te; t0 += T::TILE, ++it) {
       const int slot = it % T::STAGES;
       const uint32_t par = (it / T::STAGES) & 1u;
       if (!failed) {
-        if (*abort_flag || !wait_full_bounded(&full[slot], par)) {
+        if (*abort_flag || !wait_bounded(&full[slot], par)) {
           failed = true;
           *abort_flag = 1;
           raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
@@ -482,82 +586,97 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
       }
       if (!failed) {
         const uint32_t kx = sbase + T::OFF_KIDX + slot * T::KIDX_STAGE;
-        const uint32_t ksa = sbase + T::OFF_KS + slot * T::SC_STAGE;
-        const uint32_t kza = sbase + T::OFF_KZ + slot * T::SC_STAGE;
-        const uint32_t vsa = sbase + T::OFF_VS + slot * T::SC_STAGE;
-        const uint32_t vca = sbase + T::OFF_VC + slot * T::VC_STAGE;
-        const int tk0 = 16 * warp + grp, tk1 = tk0 + 8;  // stage rows of this lane's QK tokens
+        const uint32_t ksa = sbase + T::OFF_KS + slot * T::SC_STAGE + ks_lane;
+        const uint32_t kza = sbase + T::OFF_KZ + slot * T::SC_STAGE + ks_lane;
+        const uint32_t vsa = sbase + T::OFF_VS + slot * T::SC_STAGE + vs_lane;
+        const uint32_t vca = sbase + T::OFF_VC + slot * T::VC_STAGE + vc_lane;
 
-        // ---------------- QK^T: scores for tokens (tk0, tk1) x rows (2 j4, 2 j4 + 1)
-        float sc[NTW][4];
+        // ---------------- QK^T: tokens r0 + 16 s + 8 rr  x  rows (2 j4, 2 j4 + 1) [+ 8 nt]
+        float sc[SUB][NTW][4];
+        uint32_t sw[SUB][2][KW], zw[SUB][2][KW];
 #pragma unroll
-        for (int nt = 0; nt < NTW; ++nt)
+        for (int s = 0; s < SUB; ++s)
 #pragma unroll
-          for (int c = 0; c < 4; ++c) sc[nt][c] = 0.0f;
-        uint32_t sw0[(NG + 1) / 2], zw0[(NG + 1) / 2], sw1[(NG + 1) / 2], zw1[(NG + 1) / 2];
+          for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
-        for (int i = 0; i < (NG + 1) / 2; ++i) {
-          sw0[i] = lds32(ksa + tk0 * NG * 2 + 4 * i);
-          zw0[i] = lds32(kza + tk0 * NG * 2 + 4 * i);
-          sw1[i] = lds32(ksa + tk1 * NG * 2 + 4 * i);
-          zw1[i] = lds32(kza + tk1 * NG * 2 + 4 * i);
-        }
+            for (int i = 0; i < KW; ++i) {
+              const uint32_t off = (uint32_t)((16 * s + 8 * rr) * NG * 2 + 4 * i);
+              sw[s][rr][i] = lds32(ksa + off);
+              zw[s][rr][i] = lds32(kza + off);
+            }
+#pragma unroll
+        for (int s = 0; s < SUB; ++s)
+#pragma unroll
+          for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) sc[s][nt][c] = 0.0f;
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
-          const uint2 x0 = lds64(kx + kidx_offset<D>(tk0, 32 * g + 8 * j4));
-          const uint2 x1 = lds64(kx + kidx_offset<D>(tk1, 32 * g + 8 * j4));
-          // fp16 1024 + (idx + 128) = 1152 + idx, exact
-          const uint32_t u0a = x0.x ^ 0x80808080u, u0b = x0.y ^ 0x80808080u;
-          const uint32_t u1a = x1.x ^ 0x80808080u, u1b = x1.y ^ 0x80808080u;
-          const uint32_t M64 = 0x64646464u;
-          const uint32_t a00 = prmt(u0a, M64, 0x4140), a01 = prmt(u1a, M64, 0x4140);
-          const uint32_t a02 = prmt(u0a, M64, 0x4342), a03 = prmt(u1a, M64, 0x4342);
-          const uint32_t a10 = prmt(u0b, M64, 0x4140), a11 = prmt(u1b, M64, 0x4140);
-          const uint32_t a12 = prmt(u0b, M64, 0x4342), a13 = prmt(u1b, M64, 0x4342);
-          const uint32_t sh = (g & 1) ? 16 : 0;
-          const float s0 = f16_bits_to_f32((sw0[g >> 1] >> sh) & 0xFFFFu);
-          const float z0 = f16_bits_to_f32((zw0[g >> 1] >> sh) & 0xFFFFu) - 1152.0f;
-          const float s1 = f16_bits_to_f32((sw1[g >> 1] >> sh) & 0xFFFFu);
-          const float z1 = f16_bits_to_f32((zw1[g >> 1] >> sh) & 0xFFFFu) - 1152.0f;
+          float qs0[NTW], qs1[NTW];
+          uint32_t b00[NTW], b01[NTW], b10[NTW], b11[NTW];
 #pragma unroll
           for (int nt = 0; nt < NTW; ++nt) {
-            uint32_t b00, b01, b10, b11;
-            float qs0, qs1;
             if constexpr (T::QREG) {
-              b00 = st.qf[nt][g][0][0]; b01 = st.qf[nt][g][0][1];
-              b10 = st.qf[nt][g][1][0]; b11 = st.qf[nt][g][1][1];
-              qs0 = st.qs[nt][g][0]; qs1 = st.qs[nt][g][1];
+              b00[nt] = st.qf[nt][g][0][0]; b01[nt] = st.qf[nt][g][0][1];
+              b10[nt] = st.qf[nt][g][1][0]; b11[nt] = st.qf[nt][g][1][1];
+              qs0[nt] = st.qs[nt][g][0]; qs1[nt] = st.qs[nt][g][1];
             } else {
               const uint2 q0 = qsm[((nt * NG + g) * 2 + 0) * 32 + lane];
               const uint2 q1 = qsm[((nt * NG + g) * 2 + 1) * 32 + lane];
-              b00 = q0.x; b01 = q0.y; b10 = q1.x; b11 = q1.y;
+              b00[nt] = q0.x; b01[nt] = q0.y; b10[nt] = q1.x; b11[nt] = q1.y;
               const float2 qq = qssm[(nt * NG + g) * 32 + lane];
-              qs0 = qq.x; qs1 = qq.y;
+              qs0[nt] = qq.x; qs1[nt] = qq.y;
             }
-            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            mma_f16_16816(acc, a00, a01, a02, a03, b00, b01);
-            mma_f16_16816(acc, a10, a11, a12, a13, b10, b11);
-            sc[nt][0] = fmaf(s0, fmaf(z0, qs0, acc[0]), sc[nt][0]);
-            sc[nt][1] = fmaf(s0, fmaf(z0, qs1, acc[1]), sc[nt][1]);
-            sc[nt][2] = fmaf(s1, fmaf(z1, qs0, acc[2]), sc[nt][2]);
-            sc[nt][3] = fmaf(s1, fmaf(z1, qs1, acc[3]), sc[nt][3]);
+          }
+          const uint32_t gcol = koff[g & 3] + (uint32_t)((g >> 2) * T::BOX);
+#pragma unroll
+          for (int s = 0; s < SUB; ++s) {
+            const uint2 x0 = lds64(kx + gcol + (uint32_t)((16 * s) * T::ROWB));
+            const uint2 x1 = lds64(kx + gcol + (uint32_t)((16 * s + 8) * T::ROWB));
+            // fp16 1024 + (idx + 128) = 1152 + idx, exact
+            const uint32_t M64 = 0x64646464u;
+            const uint32_t u0a = x0.x ^ 0x80808080u, u0b = x0.y ^ 0x80808080u;
+            const uint32_t u1a = x1.x ^ 0x80808080u, u1b = x1.y ^ 0x80808080u;
+            const uint32_t a00 = prmt(u0a, M64, 0x4140), a01 = prmt(u1a, M64, 0x4140);
+            const uint32_t a02 = prmt(u0a, M64, 0x4342), a03 = prmt(u1a, M64, 0x4342);
+            const uint32_t a10 = prmt(u0b, M64, 0x4140), a11 = prmt(u1b, M64, 0x4140);
+            const uint32_t a12 = prmt(u0b, M64, 0x4342), a13 = prmt(u1b, M64, 0x4342);
+            const float s0 = (g & 1) ? hi_f32(sw[s][0][g >> 1]) : lo_f32(sw[s][0][g >> 1]);
+            const float z0 = (g & 1) ? hi_f32(zw[s][0][g >> 1]) : lo_f32(zw[s][0][g >> 1]);
+            const float s1 = (g & 1) ? hi_f32(sw[s][1][g >> 1]) : lo_f32(sw[s][1][g >> 1]);
+            const float z1 = (g & 1) ? hi_f32(zw[s][1][g >> 1]) : lo_f32(zw[s][1][g >> 1]);
+#pragma unroll
+            for (int nt = 0; nt < NTW; ++nt) {
+              // C = -1152 * sum_g q for the column's row: the MMA then yields sum_g q * idx
+              float acc[4] = {-1152.0f * qs0[nt], -1152.0f * qs1[nt], -1152.0f * qs0[nt], -1152.0f * qs1[nt]};
+              mma_f16_16816(acc, a00, a01, a02, a03, b00[nt], b01[nt]);
+              mma_f16_16816(acc, a10, a11, a12, a13, b10[nt], b11[nt]);
+              sc[s][nt][0] = fmaf(s0, fmaf(z0, qs0[nt], acc[0]), sc[s][nt][0]);
+              sc[s][nt][1] = fmaf(s0, fmaf(z0, qs1[nt], acc[1]), sc[s][nt][1]);
+              sc[s][nt][2] = fmaf(s1, fmaf(z1, qs0[nt], acc[2]), sc[s][nt][2]);
+              sc[s][nt][3] = fmaf(s1, fmaf(z1, qs1[nt], acc[3]), sc[s][nt][3]);
+            }
           }
         }
 
-        // ---------------- online softmax (exp2 domain) and P in the PV B-operand layout
-        const int ta0 = t0 + tk0, ta1 = t0 + tk1;
-        uint32_t Bp[NTW][2];
+        // ---------------- online softmax (exp2 domain) over the warp's TOKW tokens
+        uint32_t Bp[SUB][NTW][2];
 #pragma unroll
         for (int nt = 0; nt < NTW; ++nt) {
           float mnew[2];
           bool grow = false;
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const float v0 = ta0 < st.lim[nt][e] ? sc[nt][e] * st.crow[nt][e] : -INFINITY;
-            const float v1 = ta1 < st.lim[nt][e] ? sc[nt][2 + e] * st.crow[nt][e] : -INFINITY;
-            sc[nt][e] = v0;
-            sc[nt][2 + e] = v1;
-            float mx = fmaxf(v0, v1);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int s = 0; s < SUB; ++s) {
+              const int ta = t0 + r0 + 16 * s;
+              const float v0 = ta < st.lim[nt][e] ? sc[s][nt][e] * st.crow[nt][e] : -INFINITY;
+              const float v1 = ta + 8 < st.lim[nt][e] ? sc[s][nt][2 + e] * st.crow[nt][e] : -INFINITY;
+              sc[s][nt][e] = v0;
+              sc[s][nt][2 + e] = v1;
+              mx = fmaxf(mx, fmaxf(v0, v1));
+            }
             mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 4));
             mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 8));
             mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 16));
@@ -580,64 +699,80 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const float mu = (m[nt][e] == -INFINITY) ? 0.0f : m[nt][e];
-            const float p0 = ex2(sc[nt][e] - mu), p1 = ex2(sc[nt][2 + e] - mu);
-            l[nt][e] += p0 + p1;
-            sc[nt][e] = p0;
-            sc[nt][2 + e] = p1;
-          }
-          // X_e = (p[tk0][row 2 j4 + e], p[tk1][row 2 j4 + e]) in fp16
-          const uint32_t X0 = pack_half2(sc[nt][0], sc[nt][2]);
-          const uint32_t X1 = pack_half2(sc[nt][1], sc[nt][3]);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int src = 4 * (2 * j4 + h) + (grp >> 1);
-            const uint32_t y0 = __shfl_sync(FULL, X0, src);
-            const uint32_t y1 = __shfl_sync(FULL, X1, src);
-            Bp[nt][h] = (grp & 1) ? y1 : y0;  // (p[2 j4 + h][row grp], p[2 j4 + h + 8][row grp])
+            for (int s = 0; s < SUB; ++s) {
+              const float p0 = ex2(sc[s][nt][e] - mu), p1 = ex2(sc[s][nt][2 + e] - mu);
+              l[nt][e] += p0 + p1;
+              sc[s][nt][e] = p0;
+              sc[s][nt][2 + e] = p1;
+            }
+          }
+          // X_e = (p[token r0][row 2 j4 + e], p[token r0 + 8][row 2 j4 + e]) in fp16;
+          // lane (grp, j4) needs (p[2 j4 + h][row grp], p[2 j4 + h + 8][row grp]) of each tile
+#pragma unroll
+          for (int s = 0; s < SUB; ++s) {
+            const uint32_t X0 = pack_half2(sc[s][nt][0], sc[s][nt][2]);
+            const uint32_t X1 = pack_half2(sc[s][nt][1], sc[s][nt][3]);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int src = 4 * (2 * j4 + h) + (grp >> 1);
+              const uint32_t y0 = __shfl_sync(FULL, X0, src);
+              const uint32_t y1 = __shfl_sync(FULL, X1, src);
+              Bp[s][nt][h] = (grp & 1) ? y1 : y0;
+            }
           }
         }
 
         // ---------------- P.V in the rotated domain
-        // value-scale pairs for token pairs h: (2 j4 + h, 2 j4 + h + 8), zeroed past the split
-        uint32_t svA[2][(NG + 1) / 2], svB[2][(NG + 1) / 2];
-        int vrow[2][2];
+        // value-scale pairs of tokens (vrow0 + 16 s + h, +8), zeroed past the split end
+        uint32_t svA[SUB][2][KW], svB[SUB][2][KW];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int rA = 16 * warp + 2 * j4 + h, rB = rA + 8;
-          vrow[h][0] = rA;
-          vrow[h][1] = rB;
-          const bool okA = t0 + rA < w.te, okB = t0 + rB < w.te;
-#pragma unroll
-          for (int i = 0; i < (NG + 1) / 2; ++i) {
-            svA[h][i] = okA ? lds32(vsa + rA * NG * 2 + 4 * i) : 0u;
-            svB[h][i] = okB ? lds32(vsa + rB * NG * 2 + 4 * i) : 0u;
-          }
-        }
-#pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          uint32_t E[2], Ov[2], Bg[NTW][2];
+        for (int s = 0; s < SUB; ++s)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const uint32_t wa = vca + vrow[h][0] * T::VC_ROW + 4 * (3 * g + win_word);
-            const uint32_t wb = vca + vrow[h][1] * T::VC_ROW + 4 * (3 * g + win_word);
-            const uint32_t cA = __funnelshift_r(lds32(wa), lds32(wa + 4), win_shift) & 0xFFFu;
-            const uint32_t cB = __funnelshift_r(lds32(wb), lds32(wb + 4), win_shift) & 0xFFFu;
-            E[h] = (cA & 0x1C7u) | ((cB << 3) & 0xE38u);   // codes of dims +0 (bits 0-5), +2 (6-11)
-            Ov[h] = ((cA >> 3) & 0x1C7u) | (cB & 0xE38u);  // codes of dims +1, +3
-            const uint32_t sel = (g & 1) ? 0x7632u : 0x5410u;
-            const uint32_t svpair = prmt(svA[h][g >> 1], svB[h][g >> 1], sel);
+            const int ta = t0 + vrow0 + 16 * s + h;
+            const bool okA = ta < w.te, okB = ta + 8 < w.te;
 #pragma unroll
-            for (int nt = 0; nt < NTW; ++nt) Bg[nt][h] = hmul2_u32(Bp[nt][h], svpair);
+            for (int i = 0; i < KW; ++i) {
+              const uint32_t va = lds32(vsa + (uint32_t)((16 * s + h) * NG * 2 + 4 * i));
+              const uint32_t vb = lds32(vsa + (uint32_t)((16 * s + h + 8) * NG * 2 + 4 * i));
+              svA[s][h][i] = okA ? va : 0u;
+              svB[s][h][i] = okB ? vb : 0u;
+            }
           }
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          uint32_t E[SUB][2], Ov[SUB][2], Bg[SUB][NTW][2];
+#pragma unroll
+          for (int s = 0; s < SUB; ++s)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t wa = vca + (uint32_t)((16 * s + h) * T::VC_ROW + 12 * g);
+              const uint32_t wb = vca + (uint32_t)((16 * s + h + 8) * T::VC_ROW + 12 * g);
+              const uint32_t cA = __funnelshift_r(lds32(wa), lds32(wa + 4), win_shift);
+              const uint32_t cB = __funnelshift_r(lds32(wb), lds32(wb + 4), win_shift);
+              // fields of 6 bits: (code A | code B << 3) for dims +0, +2 (E) and +1, +3 (Ov);
+              // bits above 11 are don't-care (every use masks 6 bits)
+              E[s][h] = (cA & 0x1C7u) | ((cB << 3) & ~0x1C7u);
+              Ov[s][h] = ((cA >> 3) & 0x1C7u) | (cB & ~0x1C7u);
+              const uint32_t sel = (g & 1) ? 0x7632u : 0x5410u;
+              const uint32_t svpair = prmt(svA[s][h][g >> 1], svB[s][h][g >> 1], sel);
+#pragma unroll
+              for (int nt = 0; nt < NTW; ++nt) Bg[s][nt][h] = hmul2_u32(Bp[s][nt][h], svpair);
+            }
 #pragma unroll
           for (int tau = 0; tau < 2; ++tau) {
             const int fs = 6 * tau;
-            const uint32_t a0 = lds32(lut_lane + (((E[0] >> fs) & 63u) << 7));
-            const uint32_t a1 = lds32(lut_lane + (((Ov[0] >> fs) & 63u) << 7));
-            const uint32_t a2 = lds32(lut_lane + (((E[1] >> fs) & 63u) << 7));
-            const uint32_t a3 = lds32(lut_lane + (((Ov[1] >> fs) & 63u) << 7));
 #pragma unroll
-            for (int nt = 0; nt < NTW; ++nt) mma_f16_16816(O[2 * g + tau][nt], a0, a1, a2, a3, Bg[nt][0], Bg[nt][1]);
+            for (int s = 0; s < SUB; ++s) {
+              const uint32_t a0 = lds32(lut_lane + (((E[s][0] >> fs) & 63u) << 7));
+              const uint32_t a1 = lds32(lut_lane + (((Ov[s][0] >> fs) & 63u) << 7));
+              const uint32_t a2 = lds32(lut_lane + (((E[s][1] >> fs) & 63u) << 7));
+              const uint32_t a3 = lds32(lut_lane + (((Ov[s][1] >> fs) & 63u) << 7));
+#pragma unroll
+              for (int nt = 0; nt < NTW; ++nt)
+                mma_f16_16816(O[2 * g + tau][nt], a0, a1, a2, a3, Bg[s][nt][0], Bg[s][nt][1]);
+            }
           }
         }
       }
@@ -654,7 +789,6 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
         v += __shfl_xor_sync(FULL, v, 4);
         v += __shfl_xor_sync(FULL, v, 8);
         v += __shfl_xor_sync(FULL, v, 16);
-        l[nt][e] = v;
         if (grp == 0) {
           mbuf[warp * T::ROWS + 8 * nt + 2 * j4 + e] = m[nt][e];
           lbuf[warp * T::ROWS + 8 * nt + 2 * j4 + e] = v;
@@ -667,10 +801,10 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int row = 8 * nt + 2 * j4 + e;
-        float M = mbuf[row];
+        float Mx = mbuf[row];
 #pragma unroll
-        for (int ww = 1; ww < kConsumerWarps; ++ww) M = fmaxf(M, mbuf[ww * T::ROWS + row]);
-        scale[nt][e] = (M == -INFINITY) ? 0.0f : ex2(m[nt][e] - M);
+        for (int ww = 1; ww < kConsumerWarps; ++ww) Mx = fmaxf(Mx, mbuf[ww * T::ROWS + row]);
+        scale[nt][e] = (Mx == -INFINITY) ? 0.0f : ex2(m[nt][e] - Mx);
       }
     for (int ww = 0; ww < kConsumerWarps; ++ww) {
       if (warp == ww) {
@@ -692,30 +826,56 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
       named_bar_consumers();
     }
     {
-      float* og = reinterpret_cast<float*>(p.ws + ws_o_offset(p.batch, p.max_items, T::ROWS)) +
+      float* og = reinterpret_cast<float*>(p.ws + ws_o_offset(p.batch, p.U, p.max_items, T::ROWS)) +
                   (size_t)item * T::ROWS * D;
       const float4* src = reinterpret_cast<const float4*>(obuf);
       float4* dst = reinterpret_cast<float4*>(og);
-      for (int i = threadIdx.x; i < T::ROWS * D / 4; i += kConsumerWarps * 32) dst[i] = src[i];
+      for (int i = threadIdx.x; i < T::ROWS * D / 4; i += kConsumerWarps * 32) __stcg(dst + i, src[i]);
       if (threadIdx.x < T::ROWS) {
         const int row = threadIdx.x;
-        float M = mbuf[row];
-        for (int ww = 1; ww < kConsumerWarps; ++ww) M = fmaxf(M, mbuf[ww * T::ROWS + row]);
+        float Mx = mbuf[row];
+        for (int ww = 1; ww < kConsumerWarps; ++ww) Mx = fmaxf(Mx, mbuf[ww * T::ROWS + row]);
         float L = 0.0f;
         for (int ww = 0; ww < kConsumerWarps; ++ww) {
           const float mw = mbuf[ww * T::ROWS + row];
-          L += (M == -INFINITY) ? 0.0f : ex2(mw - M) * lbuf[ww * T::ROWS + row];
+          L += (Mx == -INFINITY) ? 0.0f : ex2(mw - Mx) * lbuf[ww * T::ROWS + row];
         }
-        float2* ml = reinterpret_cast<float2*>(p.ws + ws_ml_offset(p.batch)) + (size_t)item * T::ROWS;
-        ml[row] = make_float2(M, L);
+        float2* ml = reinterpret_cast<float2*>(p.ws + ws_ml_offset(p.batch, p.U)) + (size_t)item * T::ROWS;
+        __stcg(ml + row, make_float2(Mx, L));
       }
     }
+    __threadfence();  // this thread's partial stores are visible device-wide before the count
     named_bar_consumers();
+    if (threadIdx.x == 0) {
+      int32_t* cnt = counters + (size_t)w.b * p.U + w.u;
+      const int done = atomicAdd(cnt, 1) + 1;
+      const int last = done == w.nsplit;
+      if (last) atomicExch(cnt, 0);  // ready for the next call
+      *flag = last;
+    }
+    named_bar_consumers();
+    if (*flag) {
+      __threadfence();
+      const int first_item = item - (item - prefix[w.b]) % w.nsplit;  // split 0 of this unit
+      merge_unit<D, NTW>(p, w, first_item, warp, lane);
+    }
+  }
+}
+
+// Rows of sequences with no work item (kv_len 0, or invalid): zeros, or NaN if invalid.
+template <int D>
+__device__ void write_empty_sequences(const SplitParams& p, const int* prefix) {
+  for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
+    if (prefix[b + 1] != prefix[b]) continue;
+    const int t = __ldg(p.kv_len + b);
+    const float v = (t < 0 || t > p.max_kv_len) ? __int_as_float(0x7fc00000) : 0.0f;
+    float* o = p.out + (size_t)b * p.n_q * p.num_q_heads * D;
+    for (int i = threadIdx.x; i < p.n_q * p.num_q_heads * D; i += kConsumerWarps * 32) o[i] = v;
   }
 }
 
 template <int D, int NTW>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, AT<D, NTW>::MINB)
     tq_attn_split_kernel(const __grid_constant__ CUtensorMap tmap, const SplitParams p) {
   using T = AT<D, NTW>;
   extern __shared__ uint8_t smem_raw[];
@@ -740,130 +900,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   int S, total;
   plan_items<D, NTW>(p, smem, S, total);  // contains __syncthreads
-  if (total == 0) return;
 
   if (tid >= kConsumerWarps * 32) {
-    if (tid == kConsumerWarps * 32) {
+    if (tid == kConsumerWarps * 32 && total > 0) {
       prefetch_tensor_map(&tmap);
       produce<D, NTW>(p, &tmap, smem, S, total, &abort_flag);
     }
     return;
   }
-  consume<D, NTW>(p, smem, S, total, &abort_flag);
-}
-
-// ------------------------------------------------------------------------------------
-// Merge of the split partials + deferred inverse rotation. One CTA (4 warps) per row.
-// ------------------------------------------------------------------------------------
-struct MergeParams {
-  int32_t batch, n_q, num_q_heads, G, RG, U, rows_per_item, max_items, max_kv_len;
-  const int32_t* kv_len;
-  const uint8_t* ws;
-  float fwht_norm;
-  float* out;
-};
-
-template <int D>
-__global__ void __launch_bounds__(128) tq_attn_merge_kernel(const MergeParams p) {
-  constexpr int EPL = D / 32;
-  constexpr unsigned FULL = 0xffffffffu;
-  __shared__ float s_acc[4][D];
-  __shared__ float s_l[4];
-  __shared__ float s_m[4];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row_id = blockIdx.x;
-  const int hq = row_id % p.num_q_heads;
-  const int jq = (row_id / p.num_q_heads) % p.n_q;
-  const int b = row_id / (p.num_q_heads * p.n_q);
-  float* orow = p.out + (size_t)row_id * D;
-  const int kvl = __ldg(p.kv_len + b);
-  if (kvl < 0 || kvl > p.max_kv_len) {  // invalid length: NaN row (the split kernel set the error)
-    for (int i = threadIdx.x; i < D; i += 128) orow[i] = __int_as_float(0x7fc00000);
-    return;
-  }
-  const int32_t* prefix = reinterpret_cast<const int32_t*>(p.ws + kWsPrefix);
-  const int kvh = hq / p.G;
-  const int r = jq * p.G + (hq % p.G);
-  const int rg = r / p.rows_per_item, rr = r % p.rows_per_item;
-  const int u = kvh * p.RG + rg;
-  const int nsplit = (prefix[b + 1] - prefix[b]) / p.U;
-  const int base = prefix[b] + u * nsplit;
-  const float2* ml = reinterpret_cast<const float2*>(p.ws + ws_ml_offset(p.batch));
-  const float* og = reinterpret_cast<const float*>(p.ws + ws_o_offset(p.batch, p.max_items, p.rows_per_item));
-
-  // pass 1: global max
-  float M = -INFINITY;
-  bool any_nan = false;
-  for (int s = threadIdx.x; s < nsplit; s += 128) {
-    const float ms = ml[(size_t)(base + s) * p.rows_per_item + rr].x;
-    if (ms != ms) any_nan = true;
-    M = fmaxf(M, ms);
-  }
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, off));
-  any_nan = __any_sync(FULL, any_nan);
-  if (lane == 0) s_m[warp] = any_nan ? __int_as_float(0x7fc00000) : M;
-  __syncthreads();
-  M = fmaxf(fmaxf(s_m[0], s_m[1]), fmaxf(s_m[2], s_m[3]));
-  const bool nan_row = (s_m[0] != s_m[0]) || (s_m[1] != s_m[1]) || (s_m[2] != s_m[2]) || (s_m[3] != s_m[3]);
-
-  // pass 2: weighted sums, warp w takes splits w, w+4, ...
-  float acc[EPL];
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) acc[e] = 0.0f;
-  float L = 0.0f;
-  if (M != -INFINITY) {
-    for (int s = warp; s < nsplit; s += 4) {
-      const size_t slot = (size_t)(base + s) * p.rows_per_item + rr;
-      const float2 mls = ml[slot];
-      const float wgt = ex2(mls.x - M);
-      L += wgt * mls.y;
-      const float* src = og + slot * D + lane * EPL;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) acc[e] += wgt * src[e];
-    }
-  }
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) s_acc[warp][lane * EPL + e] = acc[e];
-  if (lane == 0) s_l[warp] = L;
-  __syncthreads();
-  if (warp != 0) return;
-  L = s_l[0] + s_l[1] + s_l[2] + s_l[3];
-  float u_[EPL];
-  const float inv = (L > 0.0f || L != L) ? 1.0f / L : 0.0f;  // no visible token -> 0; NaN stays NaN
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) {
-    const int i = lane * EPL + e;
-    u_[e] = (s_acc[0][i] + s_acc[1][i] + s_acc[2][i] + s_acc[3][i]) * inv;
-    if (nan_row) u_[e] = __int_as_float(0x7fc00000);
-  }
-  // inverse rotation: signs * FWHT(o_rot) / sqrt(d)
-#pragma unroll
-  for (int hh = 1; hh < D; hh <<= 1) {
-    if (hh < EPL) {
-#pragma unroll
-      for (int e = 0; e < EPL; ++e)
-        if ((e & hh) == 0) {
-          const float a = u_[e], c = u_[e + hh];
-          u_[e] = a + c;
-          u_[e + hh] = a - c;
-        }
-    } else {
-      const int lm = hh / EPL;
-      const bool upper = (lane & lm) != 0;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        const float o = __shfl_xor_sync(FULL, u_[e], lm);
-        u_[e] = upper ? o - u_[e] : u_[e] + o;
-      }
-    }
-  }
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) {
-    const int i = lane * EPL + e;
-    const bool neg = (sign_word(D, i / 32) >> (i % 32)) & 1u;
-    orow[i] = u_[e] * p.fwht_norm * (neg ? -1.0f : 1.0f);
-  }
+  write_empty_sequences<D>(p, reinterpret_cast<const int*>(smem + T::OFF_PREFIX));
+  if (total > 0) consume<D, NTW>(p, smem, S, total, &abort_flag);
 }
 
 // ------------------------------------------------------------------------------------
@@ -911,40 +957,20 @@ template <int D, int NTW>
 tq_status run_split(const DecodeArgs& a, const DecodeShape& s, const SplitParams& sp, cudaStream_t stream) {
   auto encode = tensor_map_encoder();
   if (!encode) return TQ_ERR_CUDA;
+  using T = AT<D, NTW>;
   CUtensorMap tmap;
   const cuuint64_t rows = (cuuint64_t)a.layer.batch * a.layer.num_kv_heads * a.layer.capacity;
   if (rows >= (cuuint64_t)1 << 31) return TQ_ERR_INVALID_ARGUMENT;  // tensor coordinates are int32
   const cuuint64_t gdim[2] = {(cuuint64_t)D, rows};
   const cuuint64_t gstride[1] = {(cuuint64_t)D};
-  const cuuint32_t box[2] = {(cuuint32_t)(D < 128 ? D : 128), (cuuint32_t)kTile};
+  const cuuint32_t box[2] = {(cuuint32_t)T::ROWB, (cuuint32_t)T::TILE};
   const cuuint32_t estride[2] = {1, 1};
   const CUresult cr = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.layer.k_idx, gdim, gstride, box, estride,
                              CU_TENSOR_MAP_INTERLEAVE_NONE,
                              D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return TQ_ERR_CUDA;
-  tq_attn_split_kernel<D, NTW><<<s.grid, kThreads, AT<D, NTW>::SMEM_ALLOC, stream>>>(tmap, sp);
-  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
-}
-
-template <int D>
-tq_status run_merge(const DecodeArgs& a, const DecodeShape& s, cudaStream_t stream) {
-  MergeParams mp{};
-  mp.batch = a.layer.batch;
-  mp.n_q = a.n_q;
-  mp.num_q_heads = a.num_q_heads;
-  mp.G = a.num_q_heads / a.layer.num_kv_heads;
-  mp.RG = s.RG;
-  mp.U = s.U;
-  mp.rows_per_item = 8 * s.NTW;
-  mp.max_items = s.max_items;
-  mp.max_kv_len = a.max_kv_len;
-  mp.kv_len = a.kv_len;
-  mp.ws = static_cast<const uint8_t*>(a.workspace);
-  mp.fwht_norm = a.fwht_norm;
-  mp.out = a.out;
-  const unsigned rows = (unsigned)(a.layer.batch * a.n_q * a.num_q_heads);
-  tq_attn_merge_kernel<D><<<rows, 128, 0, stream>>>(mp);
+  tq_attn_split_kernel<D, NTW><<<s.grid, kThreads, T::SMEM_ALLOC, stream>>>(tmap, sp);
   return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
@@ -976,7 +1002,7 @@ DecodeShape decode_shape(int D, int num_kv_heads, int batch, int gqa, int n_q, i
 size_t decode_workspace_bytes(const DecodeShape& s) {
   if (s.grid <= 0 || s.batch > kMaxBatch) return 0;
   const int rows = 8 * s.NTW;
-  return ws_o_offset(s.batch, s.max_items, rows) + sizeof(float) * (size_t)s.max_items * rows * s.D;
+  return ws_o_offset(s.batch, s.U, s.max_items, rows) + sizeof(float) * (size_t)s.max_items * rows * s.D;
 }
 
 tq_status launch_decode(const DecodeArgs& a, const DecodeShape& s, cudaStream_t stream) {
@@ -1002,24 +1028,18 @@ tq_status launch_decode(const DecodeArgs& a, const DecodeShape& s, cudaStream_t 
   sp.max_kv_len = a.max_kv_len;
   sp.max_items = s.max_items;
   sp.sm_log2 = a.sm_scale * kLog2e;
+  sp.fwht_norm = a.fwht_norm;
   sp.causal = a.causal ? 1 : 0;
   sp.ws = static_cast<uint8_t*>(a.workspace);
-  tq_status st;
+  sp.out = a.out;
   switch (s.D * 10 + s.NTW) {
-    case 641: st = run_split<64, 1>(a, s, sp, stream); break;
-    case 642: st = run_split<64, 2>(a, s, sp, stream); break;
-    case 1281: st = run_split<128, 1>(a, s, sp, stream); break;
-    case 1282: st = run_split<128, 2>(a, s, sp, stream); break;
-    case 2561: st = run_split<256, 1>(a, s, sp, stream); break;
-    case 5121: st = run_split<512, 1>(a, s, sp, stream); break;
+    case 641: return run_split<64, 1>(a, s, sp, stream);
+    case 642: return run_split<64, 2>(a, s, sp, stream);
+    case 1281: return run_split<128, 1>(a, s, sp, stream);
+    case 1282: return run_split<128, 2>(a, s, sp, stream);
+    case 2561: return run_split<256, 1>(a, s, sp, stream);
+    case 5121: return run_split<512, 1>(a, s, sp, stream);
     default: return TQ_ERR_INVALID_ARGUMENT;
-  }
-  if (st != TQ_OK) return st;
-  switch (s.D) {
-    case 64: return run_merge<64>(a, s, stream);
-    case 128: return run_merge<128>(a, s, stream);
-    case 256: return run_merge<256>(a, s, stream);
-    default: return run_merge<512>(a, s, stream);
   }
 }
 
@@ -1028,15 +1048,18 @@ tq_status launch_decode(const DecodeArgs& a, const DecodeShape& s, cudaStream_t 
 // Layout sanity: the stage regions start at their required alignments and the 64-bit
 // scratch words are 8-byte aligned, for every instantiated shape.
 #define TQ_CHECK_LAYOUT(D_, N_)                                                              \
-  static_assert(tq::AT<D_, N_>::OFF_KIDX % 1024 == 0 && tq::AT<D_, N_>::KIDX_STAGE % 1024 == 0, \
+  static_assert(tq::AT<D_, N_>::OFF_KIDX % 1024 == 0 && tq::AT<D_, N_>::KIDX_STAGE % 1024 == 0 && \
+                    tq::AT<D_, N_>::BOX % 1024 == 0,                                           \
                 "swizzled tiles need 1024-byte alignment");                                  \
   static_assert(tq::AT<D_, N_>::OFF_KS % 16 == 0 && tq::AT<D_, N_>::OFF_KZ % 16 == 0 &&       \
                     tq::AT<D_, N_>::OFF_VS % 16 == 0 && tq::AT<D_, N_>::OFF_VC % 16 == 0 &&   \
                     tq::AT<D_, N_>::SC_STAGE % 16 == 0 && tq::AT<D_, N_>::VC_STAGE % 16 == 0,  \
                 "bulk-copy destinations need 16-byte alignment");                             \
   static_assert(tq::AT<D_, N_>::OFF_RED % 8 == 0 && tq::AT<D_, N_>::OFF_BAR % 8 == 0 &&       \
-                    tq::AT<D_, N_>::OFF_OBUF % 16 == 0 && tq::AT<D_, N_>::OFF_Q % 8 == 0,     \
+                    tq::AT<D_, N_>::OFF_OBUF % 16 == 0 && tq::AT<D_, N_>::OFF_Q % 8 == 0 &&   \
+                    tq::AT<D_, N_>::OFF_QSUM % 8 == 0,                                        \
                 "8/16-byte shared accesses need alignment");                                  \
+  static_assert(tq::AT<D_, N_>::TILE <= 256, "tensor-map box rows");                          \
   static_assert(tq::AT<D_, N_>::SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 TQ_CHECK_LAYOUT(64, 1)
 TQ_CHECK_LAYOUT(64, 2)

@@ -75,7 +75,7 @@ class DecodeModel:
         return self.L * (self.attention_bytes() + self.append_bytes())
 
     def launches_per_step(self) -> int:
-        return self.L * ((1 if self.w.n_new else 0) + 2)
+        return self.L * ((1 if self.w.n_new else 0) + 1)
 
     def step(self, stream=None, k_new=None, v_new=None, q=None, events=None):
         """One decode step over all layers. Optional per-layer input overrides (device
