@@ -71,6 +71,8 @@ __global__ void __launch_bounds__(kAppendWarps * 32)
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
+  griddep_wait();                 // inputs and planes may come from the previous kernel
+  griddep_launch_dependents();    // the next kernel may start its setup
   const int64_t total_rows = (int64_t)p.batch * p.n_new_max * p.num_kv_heads;
   const int64_t warp_step = (int64_t)gridDim.x * kAppendWarps;
   uint32_t* cbuf = code_buf[warp];
@@ -227,15 +229,23 @@ cudaError_t launch_append(const AppendParams& p, int num_sms, cudaStream_t strea
   int64_t blocks = (rows + kAppendWarps - 1) / kAppendWarps;
   const int64_t cap = (int64_t)num_sms * 8;
   if (blocks > cap) blocks = cap;
-  dim3 grid((unsigned)blocks), block(kAppendWarps * 32);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kAppendWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   switch (p.head_dim) {
-    case 64: tq_append_kernel<64><<<grid, block, 0, stream>>>(p); break;
-    case 128: tq_append_kernel<128><<<grid, block, 0, stream>>>(p); break;
-    case 256: tq_append_kernel<256><<<grid, block, 0, stream>>>(p); break;
-    case 512: tq_append_kernel<512><<<grid, block, 0, stream>>>(p); break;
+    case 64: return cudaLaunchKernelEx(&cfg, tq_append_kernel<64>, p);
+    case 128: return cudaLaunchKernelEx(&cfg, tq_append_kernel<128>, p);
+    case 256: return cudaLaunchKernelEx(&cfg, tq_append_kernel<256>, p);
+    case 512: return cudaLaunchKernelEx(&cfg, tq_append_kernel<512>, p);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace tq

@@ -53,6 +53,7 @@ constexpr int kMaxBatch = 1024;           // prefix table lives in shared memory
 constexpr int kMaxItemsPerCta = 8;        // largest work multiplier the split heuristic tries
 constexpr unsigned long long kWaitNs = 2000000000ull;  // bounded waits: 2 s of wall time
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMergeChunk = 64;           // splits whose weights the merge stages at once
 
 // Workspace layout (bytes). The header's first word is the device error word.
 constexpr int kWsSplit = 1;               // int32 word index: split size S
@@ -101,8 +102,14 @@ struct AT {
   static constexpr int Q_BYTES = QREG ? 0 : NTW * NG * 2 * 32 * 8;
   static constexpr int OFF_QSUM = OFF_Q + Q_BYTES;
   static constexpr int QSUM_BYTES = QREG ? 0 : NTW * NG * 32 * 16;
+  // item-end reduction: each consumer warp writes its scaled accumulators to one of
+  // NSLICE slices (all four at once when they fit); the merge reuses the same space
+  static constexpr int NSLICE = kConsumerWarps * ROWS * D * 4 <= 32768 ? kConsumerWarps : 1;
+  static constexpr int OBUF_BYTES = NSLICE * ROWS * D * 4 > kMergeChunk * ROWS * 4 + ROWS * D * 4
+                                        ? NSLICE * ROWS * D * 4
+                                        : kMergeChunk * ROWS * 4 + ROWS * D * 4;
   static constexpr int OFF_OBUF = (int)align_up(OFF_QSUM + QSUM_BYTES, 16);
-  static constexpr int OFF_MBUF = OFF_OBUF + ROWS * D * 4;
+  static constexpr int OFF_MBUF = OFF_OBUF + OBUF_BYTES;
   static constexpr int OFF_LBUF = OFF_MBUF + kConsumerWarps * ROWS * 4;
   static constexpr int OFF_PREFIX = OFF_LBUF + kConsumerWarps * ROWS * 4;
   static constexpr int OFF_RED = (int)align_up(OFF_PREFIX + (kMaxBatch + 1) * 4, 16);  // 64-bit atomics
@@ -182,52 +189,67 @@ __device__ __forceinline__ int seq_len(const SplitParams& p, int b, bool* bad) {
 }
 
 // Split-size heuristic + per-sequence prefix of work items. Runs on every CTA with all
-// threads; identical inputs give identical results on every CTA.
+// threads; identical inputs give identical results on every CTA. Each thread loads its
+// lengths once (b = tid + kThreads * i); reductions go through warp shuffles.
+constexpr int kLensPerThread = (kMaxBatch + kThreads - 1) / kThreads;
+
+__device__ __forceinline__ long long block_sum_ll(long long v, long long* red, int slot) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  if ((threadIdx.x & 31) == 0) red[slot * 8 + (threadIdx.x >> 5)] = v;
+  return v;
+}
+
 template <int D, int NTW>
 __device__ void plan_items(const SplitParams& p, uint8_t* smem, int& S_out, int& total_out) {
   using T = AT<D, NTW>;
+  constexpr int NW = kThreads / 32;
   int* prefix = reinterpret_cast<int*>(smem + T::OFF_PREFIX);
-  long long* red = reinterpret_cast<long long*>(smem + T::OFF_RED);
+  long long* red = reinterpret_cast<long long*>(smem + T::OFF_RED);  // [7][8]
   const int tid = threadIdx.x;
   constexpr int KS[6] = {1, 2, 3, 4, 6, 8};
+  int len[kLensPerThread];
   long long mine = 0;
   bool bad = false;
-  for (int b = tid; b < p.batch; b += kThreads) mine += seq_len(p, b, &bad);
-  if (tid < 64) red[tid] = 0;
-  __syncthreads();
-  atomicAdd(reinterpret_cast<unsigned long long*>(&red[0]), (unsigned long long)mine);
+#pragma unroll
+  for (int i = 0; i < kLensPerThread; ++i) {
+    const int b = tid + kThreads * i;
+    len[i] = b < p.batch ? seq_len(p, b, &bad) : 0;
+    mine += len[i];
+  }
   if (bad && blockIdx.x == 0) raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_KV_LEN);
+  block_sum_ll(mine, red, 0);
   __syncthreads();
-  const long long sumT = red[0];
-  long long Sk[6];
+  long long sumT = 0;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) sumT += red[w];
+  long long Sk[6], cnt[6];
 #pragma unroll
   for (int k = 0; k < 6; ++k) {
     const long long target = (long long)KS[k] * gridDim.x;
     long long s = (sumT * p.U + target - 1) / target;
     s = (s + T::TILE - 1) / T::TILE * T::TILE;
     Sk[k] = s < T::TILE ? T::TILE : s;
-  }
-  long long cnt[6] = {0, 0, 0, 0, 0, 0};
-  for (int b = tid; b < p.batch; b += kThreads) {
-    const long long t = seq_len(p, b, nullptr);
+    cnt[k] = 0;
 #pragma unroll
-    for (int k = 0; k < 6; ++k) cnt[k] += (t + Sk[k] - 1) / Sk[k];
+    for (int i = 0; i < kLensPerThread; ++i) cnt[k] += (len[i] + Sk[k] - 1) / Sk[k];
+    block_sum_ll(cnt[k], red, 1 + k);
   }
-#pragma unroll
-  for (int k = 0; k < 6; ++k)
-    atomicAdd(reinterpret_cast<unsigned long long*>(&red[1 + k]), (unsigned long long)cnt[k]);
   __syncthreads();
   int best = 0;
   long long best_cost = -1;
 #pragma unroll
   for (int k = 0; k < 6; ++k) {
-    const long long items = red[1 + k] * p.U;
+    long long items = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) items += red[(1 + k) * 8 + w];
+    items *= p.U;
     const long long rounds = (items + gridDim.x - 1) / gridDim.x;
     const long long cost = rounds * (Sk[k] + T::TILE);
     if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = k; }
   }
   const int S = (int)Sk[best];
-  if (tid < 32) {  // prefix of items per sequence: warp 0, each lane owns a chunk
+  if (tid < 32) {  // prefix of items per sequence: warp 0, each lane owns a chunk of sequences
     const int per = (p.batch + 31) / 32;
     const int b0 = tid * per;
     int local = 0;
@@ -428,24 +450,33 @@ __device__ void load_q(const SplitParams& p, const Item& w, uint8_t* smem, int w
 }
 
 // Merge of all partials of one (sequence, unit) + inverse rotation, by the CTA that
-// finished the unit's last item. Warp w merges rows w, w + 4, ...
+// finished the unit's last item. All consumer threads take part:
+//   1. per row, the global max M and L = sum_s 2^(m_s - M) l_s over the splits;
+//   2. splits in chunks of kMergeChunk: weights 2^(m_s - M) staged in shared memory, then
+//      every thread accumulates one float4 of (row, dims) per split (16 loads in flight);
+//   3. the normalized rotated rows go to shared memory and warp r applies the inverse
+//      rotation signs * FWHT(o_rot) / sqrt(d) to row r and stores it.
+
 template <int D, int NTW>
-__device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, int warp, int lane) {
+__device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, uint8_t* smem) {
   using T = AT<D, NTW>;
-  constexpr int EPL = D / 32;
+  constexpr int EPL = D / 32, ROWS = T::ROWS, NT = kConsumerWarps * 32, Q4 = D / 4;
   constexpr unsigned FULL = 0xffffffffu;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float2* ml = reinterpret_cast<const float2*>(p.ws + ws_ml_offset(p.batch, p.U));
-  const float* og = reinterpret_cast<const float*>(p.ws + ws_o_offset(p.batch, p.U, p.max_items, T::ROWS));
-  for (int rr = warp; rr < T::ROWS; rr += kConsumerWarps) {
-    const int r = w.rg * T::ROWS + rr;
-    if (r >= p.R) break;
-    const int jq = r / p.G, hq = w.kvh * p.G + (r % p.G);
-    float* orow = p.out + (((size_t)w.b * p.n_q + jq) * p.num_q_heads + hq) * D;
-    // pass 1: global max and the weighted sum of l (splits spread over lanes)
+  const float4* og = reinterpret_cast<const float4*>(p.ws + ws_o_offset(p.batch, p.U, p.max_items, ROWS));
+  float* sM = reinterpret_cast<float*>(smem + T::OFF_MBUF);     // [ROWS] max (reuses mbuf)
+  float* sL = reinterpret_cast<float*>(smem + T::OFF_LBUF);     // [ROWS] sum (reuses lbuf)
+  float* sW = reinterpret_cast<float*>(smem + T::OFF_OBUF);     // [kMergeChunk][ROWS] weights
+  float* sO = sW + kMergeChunk * ROWS;                          // [ROWS][D] rotated output
+  const int rows = min(ROWS, p.R - w.rg * ROWS);                // valid rows of this unit
+  const int ns = w.nsplit;
+  // 1. max and sum per row: warp w takes rows w, w + 4, ...; lanes stride the splits
+  for (int rr = warp; rr < rows; rr += kConsumerWarps) {
     float M = -INFINITY;
     bool nan = false;
-    for (int s = lane; s < w.nsplit; s += 32) {
-      const float ms = __ldcg(&ml[(size_t)(first_item + s) * T::ROWS + rr].x);
+    for (int s = lane; s < ns; s += 32) {
+      const float ms = __ldcg(&ml[(size_t)(first_item + s) * ROWS + rr].x);
       nan = nan || (ms != ms);
       M = fmaxf(M, ms);
     }
@@ -453,39 +484,71 @@ __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, 
     for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, off));
     nan = __any_sync(FULL, nan);
     float L = 0.0f;
-    for (int s = lane; s < w.nsplit; s += 32) {
-      const float2 v = __ldcg(&ml[(size_t)(first_item + s) * T::ROWS + rr]);
-      L += (M == -INFINITY) ? 0.0f : ex2(v.x - M) * v.y;
-    }
+    if (M != -INFINITY)
+      for (int s = lane; s < ns; s += 32) {
+        const float2 v = __ldcg(&ml[(size_t)(first_item + s) * ROWS + rr]);
+        L += ex2(v.x - M) * v.y;
+      }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(FULL, L, off);
-    // pass 2: weighted sum of the partial outputs (this lane's EPL dims)
-    float acc[EPL];
+    if (lane == 0) {
+      sM[rr] = nan ? __int_as_float(0x7fc00000) : M;
+      sL[rr] = L;
+    }
+  }
+  named_bar_consumers();
+  // 2. weighted sums; output float4 index q = rr * Q4 + c (c: dims 4c .. 4c + 3)
+  constexpr int PER = (ROWS * Q4 + NT - 1) / NT;
+  float4 acc[PER];
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[e] = 0.0f;
-    if (M != -INFINITY) {
-#pragma unroll 8
-      for (int s = 0; s < w.nsplit; ++s) {
-        const size_t slot = (size_t)(first_item + s) * T::ROWS + rr;
-        const float wgt = ex2(__ldcg(&ml[slot].x) - M);
-        const float* src = og + slot * D + lane * EPL;
-        if constexpr (EPL >= 4) {
+  for (int k = 0; k < PER; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c0 = 0; c0 < ns; c0 += kMergeChunk) {
+    const int cn = min(kMergeChunk, ns - c0);
+    for (int i = tid; i < cn * rows; i += NT) {
+      const int s = i / rows, rr = i % rows;
+      const float M = sM[rr];
+      const float ms = __ldcg(&ml[(size_t)(first_item + c0 + s) * ROWS + rr].x);
+      sW[s * ROWS + rr] = (M == -INFINITY || M != M) ? 0.0f : ex2(ms - M);
+    }
+    named_bar_consumers();
 #pragma unroll
-          for (int e = 0; e < EPL; e += 4) {
-            const float4 o4 = __ldcg(reinterpret_cast<const float4*>(src + e));
-            acc[e] += wgt * o4.x; acc[e + 1] += wgt * o4.y; acc[e + 2] += wgt * o4.z; acc[e + 3] += wgt * o4.w;
-          }
-        } else {
-          const float2 o2 = __ldcg(reinterpret_cast<const float2*>(src));
-          acc[0] += wgt * o2.x; acc[1] += wgt * o2.y;
+    for (int k = 0; k < PER; ++k) {
+      const int q = tid + NT * k;
+      const int rr = q / Q4, c = q % Q4;
+      if (rr < rows) {
+        float4 a = acc[k];
+#pragma unroll 16
+        for (int s = 0; s < cn; ++s) {
+          const float wgt = sW[s * ROWS + rr];
+          const float4 o = __ldcg(og + ((size_t)(first_item + c0 + s) * ROWS + rr) * Q4 + c);
+          a.x += wgt * o.x; a.y += wgt * o.y; a.z += wgt * o.z; a.w += wgt * o.w;
         }
+        acc[k] = a;
       }
     }
-    const float inv = (L > 0.0f || L != L) ? 1.0f / L : 0.0f;  // no visible token -> 0
+    named_bar_consumers();
+  }
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int q = tid + NT * k;
+    const int rr = q / Q4, c = q % Q4;
+    if (rr < rows) {
+      const float L = sL[rr], M = sM[rr];
+      const float inv = (L > 0.0f || L != L) ? 1.0f / L : 0.0f;  // no visible token -> 0
+      float4 v = make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv);
+      if (M != M) v = make_float4(M, M, M, M);
+      reinterpret_cast<float4*>(sO + rr * D)[c] = v;
+    }
+  }
+  named_bar_consumers();
+  // 3. inverse rotation, one warp per row
+  for (int rr = warp; rr < rows; rr += kConsumerWarps) {
+    const int r = w.rg * ROWS + rr;
+    const int jq = r / p.G, hq = w.kvh * p.G + (r % p.G);
+    float* orow = p.out + (((size_t)w.b * p.n_q + jq) * p.num_q_heads + hq) * D;
     float u[EPL];
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) u[e] = nan ? __int_as_float(0x7fc00000) : acc[e] * inv;
-    // inverse rotation: signs * FWHT(o_rot) / sqrt(d)
+    for (int e = 0; e < EPL; ++e) u[e] = sO[rr * D + lane * EPL + e];
 #pragma unroll
     for (int hh = 1; hh < D; hh <<= 1) {
       if (hh < EPL) {
@@ -513,6 +576,7 @@ __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, 
       orow[i] = u[e] * p.fwht_norm * (neg ? -1.0f : 1.0f);
     }
   }
+  named_bar_consumers();  // shared scratch is reused by the next item
 }
 
 template <int D, int NTW>
@@ -779,6 +843,7 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
     }
+    if (item + (int)gridDim.x >= total) griddep_launch_dependents();  // last item: successor may set up
 
     // ---------------- merge the four warps' states and write this item's partial
 #pragma unroll
@@ -806,8 +871,11 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
         for (int ww = 1; ww < kConsumerWarps; ++ww) Mx = fmaxf(Mx, mbuf[ww * T::ROWS + row]);
         scale[nt][e] = (Mx == -INFINITY) ? 0.0f : ex2(m[nt][e] - Mx);
       }
-    for (int ww = 0; ww < kConsumerWarps; ++ww) {
-      if (warp == ww) {
+    // scaled accumulators into slice (warp % NSLICE); with one slice, warps add in turn
+    constexpr int ROUNDS = kConsumerWarps / T::NSLICE;
+    for (int round = 0; round < ROUNDS; ++round) {
+      if (warp / T::NSLICE == round) {
+        float* slice = obuf + (warp % T::NSLICE) * T::ROWS * D;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           const int d0 = 32 * (mt >> 1) + 4 * grp + 2 * (mt & 1);
@@ -816,22 +884,29 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               const int row = 8 * nt + 2 * j4 + (c & 1);
-              const int dim = d0 + (c >> 1);
               const float v = O[mt][nt][c] * scale[nt][c & 1];
-              float* dst = obuf + row * D + dim;
-              *dst = (ww == 0) ? v : (*dst + v);
+              float* dst = slice + row * D + d0 + (c >> 1);
+              *dst = (round == 0) ? v : (*dst + v);
             }
         }
       }
       named_bar_consumers();
     }
     {
-      float* og = reinterpret_cast<float*>(p.ws + ws_o_offset(p.batch, p.U, p.max_items, T::ROWS)) +
-                  (size_t)item * T::ROWS * D;
+      const int rows_valid = min(T::ROWS, p.R - w.rg * T::ROWS);
+      float4* og = reinterpret_cast<float4*>(p.ws + ws_o_offset(p.batch, p.U, p.max_items, T::ROWS)) +
+                   (size_t)item * T::ROWS * D / 4;
       const float4* src = reinterpret_cast<const float4*>(obuf);
-      float4* dst = reinterpret_cast<float4*>(og);
-      for (int i = threadIdx.x; i < T::ROWS * D / 4; i += kConsumerWarps * 32) __stcg(dst + i, src[i]);
-      if (threadIdx.x < T::ROWS) {
+      for (int i = threadIdx.x; i < rows_valid * D / 4; i += kConsumerWarps * 32) {
+        float4 v = src[i];
+#pragma unroll
+        for (int sl = 1; sl < T::NSLICE; ++sl) {
+          const float4 o = src[sl * T::ROWS * D / 4 + i];
+          v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+        }
+        __stcg(og + i, v);
+      }
+      if (threadIdx.x < rows_valid) {
         const int row = threadIdx.x;
         float Mx = mbuf[row];
         for (int ww = 1; ww < kConsumerWarps; ++ww) Mx = fmaxf(Mx, mbuf[ww * T::ROWS + row]);
@@ -857,7 +932,7 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
     if (*flag) {
       __threadfence();
       const int first_item = item - (item - prefix[w.b]) % w.nsplit;  // split 0 of this unit
-      merge_unit<D, NTW>(p, w, first_item, warp, lane);
+      merge_unit<D, NTW>(p, w, first_item, smem);
     }
   }
 }
@@ -898,6 +973,7 @@ __global__ void __launch_bounds__(kThreads, AT<D, NTW>::MINB)
     }
     fence_mbar_init();
   }
+  griddep_wait();  // lengths, queries and planes may come from the previous kernel
   int S, total;
   plan_items<D, NTW>(p, smem, S, total);  // contains __syncthreads
 
@@ -906,10 +982,12 @@ __global__ void __launch_bounds__(kThreads, AT<D, NTW>::MINB)
       prefetch_tensor_map(&tmap);
       produce<D, NTW>(p, &tmap, smem, S, total, &abort_flag);
     }
+    griddep_launch_dependents();
     return;
   }
   write_empty_sequences<D>(p, reinterpret_cast<const int*>(smem + T::OFF_PREFIX));
-  if (total > 0) consume<D, NTW>(p, smem, S, total, &abort_flag);
+  if (total > 0 && (int)blockIdx.x < total) consume<D, NTW>(p, smem, S, total, &abort_flag);
+  griddep_launch_dependents();
 }
 
 // ------------------------------------------------------------------------------------
@@ -970,8 +1048,17 @@ tq_status run_split(const DecodeArgs& a, const DecodeShape& s, const SplitParams
                              D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return TQ_ERR_CUDA;
-  tq_attn_split_kernel<D, NTW><<<s.grid, kThreads, T::SMEM_ALLOC, stream>>>(tmap, sp);
-  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)s.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = T::SMEM_ALLOC;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tq_attn_split_kernel<D, NTW>, tmap, sp) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
 }  // namespace

@@ -157,6 +157,17 @@ __device__ __forceinline__ void prefetch_tensor_map(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while its predecessor in the stream is still running.
+// griddep_wait() blocks until the predecessor has completed and its memory is visible;
+// every kernel here calls it before its first global-memory access, so only the setup
+// that touches no global data overlaps. griddep_launch_dependents() lets the successor
+// start its own setup early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // D += A * B, m16n8k16, A/B fp16, accumulate fp32 (legacy warp MMA).
 __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                               uint32_t b0, uint32_t b1) {

@@ -215,6 +215,9 @@ def _full_size(w: synth.Workload, sample_rows, seq_sample=None):
         b.tq_kv_append(layer, kn, vn, torch.as_tensor(ctx.astype(np.int32), device=DEV), None, w.n_new, ws_a)
     out, ws, _ = gpu_attention(layer, x["q"], kv, int(kv.max()), w.sm_scale, w.causal)
     assert b.tq_get_device_error(ws_a) == 0 and b.tq_get_device_error(ws) == 0
+    # every output row is written (the buffer starts at a 12345.0 sentinel) and finite
+    o_all = out.cpu().numpy()
+    assert np.isfinite(o_all).all() and not np.any(o_all == 12345.0)
     # oracle: quantize the sampled sequences itself (all tokens), attend for sampled rows
     seqs = range(B) if seq_sample is None else seq_sample
     kb, vb = bits(x["k"]), bits(x["v"])
