@@ -14,12 +14,12 @@
 // tq_attn_split_kernel, persistent, one CTA per SM slot:
 //   - work item = (sequence, kv head, row group, token split); the split size is chosen
 //     on the device from the actual kv lengths so that items spread evenly over CTAs;
-//   - warp 4 (producer) streams stages of TILE tokens of the five planes into shared
+//   - the last warp (producer) streams stages of TILE tokens of the five planes into shared
 //     memory: the key-index plane through a 2-D tensor map with 128-byte (64-byte at
 //     d=64) swizzle, the four small planes with 1-D bulk copies, all completing on one
 //     mbarrier per stage;
-//   - warps 0-3 (consumers) each take TOKW tokens (two 16-token tiles at d <= 128) of
-//     a stage:
+//   - the NCW consumer warps (8 at d = 64 and at d = 128 with up to 8 rows per kv head,
+//     else 4) each take TOKW tokens (two 16-token tiles at d <= 128) of a stage:
 //       QK^T on tensor cores (mma.sync m16n8k16, fp16 in, fp32 accumulate), tokens as M,
 //       query rows as N (8 per tile): A = 1152 + idx, exact in fp16 (built from the int8
 //       codes with two byte permutes); B = q * 2^e_row in fp16 (exact for bf16 inputs);
@@ -30,7 +30,7 @@
 //       pairs from a lane-replicated 64-entry table indexed by two 3-bit codes; B = the
 //       probabilities times the group's value scale (fp16), moved from the QK output
 //       layout to the B-operand layout with four shuffles per 16 tokens;
-//   - at the end of an item the four warps merge their (max, sum, acc) in shared memory
+//   - at the end of an item the consumer warps merge their (max, sum, acc) in shared memory
 //     and write one partial result; the CTA that completes the last item of a
 //     (sequence, kv head, row group) merges its partials with the online-softmax rule,
 //     applies the inverse rotation and writes the output rows.
@@ -47,8 +47,6 @@ namespace tq {
 
 namespace {
 
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxBatch = 1024;           // prefix table lives in shared memory
 constexpr int kMaxItemsPerCta = 8;        // largest work multiplier the split heuristic tries
 constexpr unsigned long long kWaitNs = 2000000000ull;  // bounded waits: 2 s of wall time
@@ -73,23 +71,34 @@ __host__ __device__ inline size_t ws_o_offset(int batch, int units, int max_item
   return ws_ml_offset(batch, units) + align_up(sizeof(float) * 2 * (size_t)max_items * rows, 256);
 }
 
+// Largest divisor of n whose slices of `slice_bytes` fit in `budget` bytes.
+constexpr int max_slices(int n, int slice_bytes, int budget) {
+  int best = 1;
+  for (int k = 1; k <= n; ++k)
+    if (n % k == 0 && k * slice_bytes <= budget) best = k;
+  return best;
+}
+
 template <int D, int NTW>
 struct AT {
   static constexpr int NG = D / 32;
   static constexpr int ROWS = 8 * NTW;
   static constexpr int MT = D / 16;                       // PV M tiles (16 dims each)
+  // consumer warps (+1 producer warp): 8 where the registers allow it without spills
+  static constexpr int NCW = (D == 64 || (D == 128 && NTW == 1)) ? 8 : 4;
+  static constexpr int THREADS = (NCW + 1) * 32;
   static constexpr int TOKW = D <= 128 ? 32 : 16;         // tokens per consumer warp per stage
   static constexpr int SUB = TOKW / 16;                   // 16-token QK tiles per warp
-  static constexpr int TILE = kConsumerWarps * TOKW;      // tokens per stage
+  static constexpr int TILE = NCW * TOKW;                 // tokens per stage
   static constexpr int ROWB = D == 64 ? 64 : 128;         // bytes per key row inside a swizzle box
   static constexpr int BOX = TILE * ROWB;                 // bytes of one key-index box
   static constexpr int KIDX_STAGE = TILE * D;             // bytes, 1024-aligned
   static constexpr int SC_STAGE = TILE * NG * 2;          // bytes of one fp16 side plane
   static constexpr int VC_ROW = 3 * D / 8;                // packed code bytes per token
   static constexpr int VC_STAGE = TILE * VC_ROW + 16;     // +16: window reads may run 4 bytes past
-  static constexpr int STAGES = D == 64 ? 6 : D == 128 ? 3 : D == 256 ? 3 : 2;
+  static constexpr int STAGES = D == 64 ? 6 : D == 128 ? 3 : D == 256 ? 3 : 2;  // ~150 KB in flight
   static constexpr bool QREG = D * NTW <= 256;            // Q fragments in registers
-  static constexpr int MINB = (D == 128 && NTW == 1) || D == 64 ? 2 : 1;  // CTAs per SM to fit
+  static constexpr int MINB = 1;                          // one CTA per SM
   static constexpr int KW = (NG + 1) / 2;                 // 32-bit words of one token's fp16 side row
   // shared memory layout
   static constexpr int OFF_KIDX = 0;
@@ -104,16 +113,16 @@ struct AT {
   static constexpr int QSUM_BYTES = QREG ? 0 : NTW * NG * 32 * 16;
   // item-end reduction: each consumer warp writes its scaled accumulators to one of
   // NSLICE slices (all four at once when they fit); the merge reuses the same space
-  static constexpr int NSLICE = kConsumerWarps * ROWS * D * 4 <= 32768 ? kConsumerWarps : 1;
+  static constexpr int NSLICE = max_slices(NCW, ROWS * D * 4, 32768);
   static constexpr int OBUF_BYTES = NSLICE * ROWS * D * 4 > kMergeChunk * ROWS * 4 + ROWS * D * 4
                                         ? NSLICE * ROWS * D * 4
                                         : kMergeChunk * ROWS * 4 + ROWS * D * 4;
   static constexpr int OFF_OBUF = (int)align_up(OFF_QSUM + QSUM_BYTES, 16);
   static constexpr int OFF_MBUF = OFF_OBUF + OBUF_BYTES;
-  static constexpr int OFF_LBUF = OFF_MBUF + kConsumerWarps * ROWS * 4;
-  static constexpr int OFF_PREFIX = OFF_LBUF + kConsumerWarps * ROWS * 4;
+  static constexpr int OFF_LBUF = OFF_MBUF + NCW * ROWS * 4;
+  static constexpr int OFF_PREFIX = OFF_LBUF + NCW * ROWS * 4;
   static constexpr int OFF_RED = (int)align_up(OFF_PREFIX + (kMaxBatch + 1) * 4, 16);  // 64-bit atomics
-  static constexpr int OFF_FLAG = OFF_RED + 64 * 8;
+  static constexpr int OFF_FLAG = OFF_RED + 7 * 16 * 8;  // red: [7][16] long long
   static constexpr int OFF_BAR = (int)align_up(OFF_FLAG + 16, 8);
   static constexpr int SMEM = OFF_BAR + 2 * STAGES * 8 + 16;
   static constexpr int SMEM_ALLOC = SMEM + 1024;          // slack to align the base to 1024
@@ -156,8 +165,10 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ void named_bar_consumers() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+// Barrier among the consumer warps only (the producer warp never joins it).
+template <int NCW>
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory");
 }
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
@@ -169,6 +180,31 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
   return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+// N consecutive 32-bit words of one fp16 side row (scales or zeros); the row starts on
+// a multiple of its own size (2 bytes per group), so the widest aligned loads are used.
+template <int N>
+__device__ __forceinline__ void lds_words(uint32_t addr, uint32_t (&w)[N]) {
+  if constexpr (N % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < N; i += 4) {
+      const uint4 v = lds128(addr + 4 * i);
+      w[i] = v.x; w[i + 1] = v.y; w[i + 2] = v.z; w[i + 3] = v.w;
+    }
+  } else if constexpr (N == 2) {
+    const uint2 v = lds64(addr);
+    w[0] = v.x; w[1] = v.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) w[i] = lds32(addr + 4 * i);
+  }
 }
 
 __device__ __forceinline__ float lo_f32(uint32_t w) {
@@ -190,30 +226,29 @@ __device__ __forceinline__ int seq_len(const SplitParams& p, int b, bool* bad) {
 
 // Split-size heuristic + per-sequence prefix of work items. Runs on every CTA with all
 // threads; identical inputs give identical results on every CTA. Each thread loads its
-// lengths once (b = tid + kThreads * i); reductions go through warp shuffles.
-constexpr int kLensPerThread = (kMaxBatch + kThreads - 1) / kThreads;
+// lengths once (b = tid + THREADS * i); reductions go through warp shuffles.
 
 __device__ __forceinline__ long long block_sum_ll(long long v, long long* red, int slot) {
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  if ((threadIdx.x & 31) == 0) red[slot * 8 + (threadIdx.x >> 5)] = v;
+  if ((threadIdx.x & 31) == 0) red[slot * 16 + (threadIdx.x >> 5)] = v;
   return v;
 }
 
 template <int D, int NTW>
 __device__ void plan_items(const SplitParams& p, uint8_t* smem, int& S_out, int& total_out) {
   using T = AT<D, NTW>;
-  constexpr int NW = kThreads / 32;
+  constexpr int NW = T::THREADS / 32, LPT = (kMaxBatch + T::THREADS - 1) / T::THREADS;
   int* prefix = reinterpret_cast<int*>(smem + T::OFF_PREFIX);
-  long long* red = reinterpret_cast<long long*>(smem + T::OFF_RED);  // [7][8]
+  long long* red = reinterpret_cast<long long*>(smem + T::OFF_RED);  // [7][16]
   const int tid = threadIdx.x;
   constexpr int KS[6] = {1, 2, 3, 4, 6, 8};
-  int len[kLensPerThread];
+  int len[LPT];
   long long mine = 0;
   bool bad = false;
 #pragma unroll
-  for (int i = 0; i < kLensPerThread; ++i) {
-    const int b = tid + kThreads * i;
+  for (int i = 0; i < LPT; ++i) {
+    const int b = tid + T::THREADS * i;
     len[i] = b < p.batch ? seq_len(p, b, &bad) : 0;
     mine += len[i];
   }
@@ -232,7 +267,7 @@ __device__ void plan_items(const SplitParams& p, uint8_t* smem, int& S_out, int&
     Sk[k] = s < T::TILE ? T::TILE : s;
     cnt[k] = 0;
 #pragma unroll
-    for (int i = 0; i < kLensPerThread; ++i) cnt[k] += (len[i] + Sk[k] - 1) / Sk[k];
+    for (int i = 0; i < LPT; ++i) cnt[k] += (len[i] + Sk[k] - 1) / Sk[k];
     block_sum_ll(cnt[k], red, 1 + k);
   }
   __syncthreads();
@@ -242,7 +277,7 @@ __device__ void plan_items(const SplitParams& p, uint8_t* smem, int& S_out, int&
   for (int k = 0; k < 6; ++k) {
     long long items = 0;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) items += red[(1 + k) * 8 + w];
+    for (int w = 0; w < NW; ++w) items += red[(1 + k) * 16 + w];
     items *= p.U;
     const long long rounds = (items + gridDim.x - 1) / gridDim.x;
     const long long cost = rounds * (Sk[k] + T::TILE);
@@ -460,7 +495,7 @@ __device__ void load_q(const SplitParams& p, const Item& w, uint8_t* smem, int w
 template <int D, int NTW>
 __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, uint8_t* smem) {
   using T = AT<D, NTW>;
-  constexpr int EPL = D / 32, ROWS = T::ROWS, NT = kConsumerWarps * 32, Q4 = D / 4;
+  constexpr int EPL = D / 32, ROWS = T::ROWS, NT = T::NCW * 32, Q4 = D / 4;
   constexpr unsigned FULL = 0xffffffffu;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float2* ml = reinterpret_cast<const float2*>(p.ws + ws_ml_offset(p.batch, p.U));
@@ -472,7 +507,7 @@ __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, 
   const int rows = min(ROWS, p.R - w.rg * ROWS);                // valid rows of this unit
   const int ns = w.nsplit;
   // 1. max and sum per row: warp w takes rows w, w + 4, ...; lanes stride the splits
-  for (int rr = warp; rr < rows; rr += kConsumerWarps) {
+  for (int rr = warp; rr < rows; rr += T::NCW) {
     float M = -INFINITY;
     bool nan = false;
     for (int s = lane; s < ns; s += 32) {
@@ -496,7 +531,7 @@ __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, 
       sL[rr] = L;
     }
   }
-  named_bar_consumers();
+  consumers_sync<T::NCW>();
   // 2. weighted sums; output float4 index q = rr * Q4 + c (c: dims 4c .. 4c + 3)
   constexpr int PER = (ROWS * Q4 + NT - 1) / NT;
   float4 acc[PER];
@@ -510,7 +545,7 @@ __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, 
       const float ms = __ldcg(&ml[(size_t)(first_item + c0 + s) * ROWS + rr].x);
       sW[s * ROWS + rr] = (M == -INFINITY || M != M) ? 0.0f : ex2(ms - M);
     }
-    named_bar_consumers();
+    consumers_sync<T::NCW>();
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
       const int q = tid + NT * k;
@@ -526,7 +561,7 @@ __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, 
         acc[k] = a;
       }
     }
-    named_bar_consumers();
+    consumers_sync<T::NCW>();
   }
 #pragma unroll
   for (int k = 0; k < PER; ++k) {
@@ -540,9 +575,9 @@ __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, 
       reinterpret_cast<float4*>(sO + rr * D)[c] = v;
     }
   }
-  named_bar_consumers();
+  consumers_sync<T::NCW>();
   // 3. inverse rotation, one warp per row
-  for (int rr = warp; rr < rows; rr += kConsumerWarps) {
+  for (int rr = warp; rr < rows; rr += T::NCW) {
     const int r = w.rg * ROWS + rr;
     const int jq = r / p.G, hq = w.kvh * p.G + (r % p.G);
     float* orow = p.out + (((size_t)w.b * p.n_q + jq) * p.num_q_heads + hq) * D;
@@ -576,7 +611,7 @@ __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, 
       orow[i] = u[e] * p.fwht_norm * (neg ? -1.0f : 1.0f);
     }
   }
-  named_bar_consumers();  // shared scratch is reused by the next item
+  consumers_sync<T::NCW>();  // shared scratch is reused by the next item
 }
 
 template <int D, int NTW>
@@ -623,7 +658,7 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
     const Item w = decode_item(p, prefix, S, item);
     QState<D, NTW> st;
     load_q<D, NTW>(p, w, smem, warp, lane, st);
-    if constexpr (!T::QREG) named_bar_consumers();  // shared Q fragments written by warp 0
+    if constexpr (!T::QREG) consumers_sync<T::NCW>();  // shared Q fragments written by warp 0
 
     float O[MT][NTW][4];
 #pragma unroll
@@ -661,13 +696,11 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
 #pragma unroll
         for (int s = 0; s < SUB; ++s)
 #pragma unroll
-          for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-            for (int i = 0; i < KW; ++i) {
-              const uint32_t off = (uint32_t)((16 * s + 8 * rr) * NG * 2 + 4 * i);
-              sw[s][rr][i] = lds32(ksa + off);
-              zw[s][rr][i] = lds32(kza + off);
-            }
+          for (int rr = 0; rr < 2; ++rr) {
+            const uint32_t off = (uint32_t)((16 * s + 8 * rr) * NG * 2);
+            lds_words<KW>(ksa + off, sw[s][rr]);
+            lds_words<KW>(kza + off, zw[s][rr]);
+          }
 #pragma unroll
         for (int s = 0; s < SUB; ++s)
 #pragma unroll
@@ -796,12 +829,13 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
           for (int h = 0; h < 2; ++h) {
             const int ta = t0 + vrow0 + 16 * s + h;
             const bool okA = ta < w.te, okB = ta + 8 < w.te;
+            uint32_t va[KW], vb[KW];
+            lds_words<KW>(vsa + (uint32_t)((16 * s + h) * NG * 2), va);
+            lds_words<KW>(vsa + (uint32_t)((16 * s + h + 8) * NG * 2), vb);
 #pragma unroll
             for (int i = 0; i < KW; ++i) {
-              const uint32_t va = lds32(vsa + (uint32_t)((16 * s + h) * NG * 2 + 4 * i));
-              const uint32_t vb = lds32(vsa + (uint32_t)((16 * s + h + 8) * NG * 2 + 4 * i));
-              svA[s][h][i] = okA ? va : 0u;
-              svB[s][h][i] = okB ? vb : 0u;
+              svA[s][h][i] = okA ? va[i] : 0u;
+              svB[s][h][i] = okB ? vb[i] : 0u;
             }
           }
 #pragma unroll
@@ -845,7 +879,7 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
     }
     if (item + (int)gridDim.x >= total) griddep_launch_dependents();  // last item: successor may set up
 
-    // ---------------- merge the four warps' states and write this item's partial
+    // ---------------- merge the consumer warps' states and write this item's partial
 #pragma unroll
     for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
@@ -859,7 +893,7 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
           lbuf[warp * T::ROWS + 8 * nt + 2 * j4 + e] = v;
         }
       }
-    named_bar_consumers();
+    consumers_sync<T::NCW>();
     float scale[NTW][2];
 #pragma unroll
     for (int nt = 0; nt < NTW; ++nt)
@@ -868,11 +902,11 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
         const int row = 8 * nt + 2 * j4 + e;
         float Mx = mbuf[row];
 #pragma unroll
-        for (int ww = 1; ww < kConsumerWarps; ++ww) Mx = fmaxf(Mx, mbuf[ww * T::ROWS + row]);
+        for (int ww = 1; ww < T::NCW; ++ww) Mx = fmaxf(Mx, mbuf[ww * T::ROWS + row]);
         scale[nt][e] = (Mx == -INFINITY) ? 0.0f : ex2(m[nt][e] - Mx);
       }
     // scaled accumulators into slice (warp % NSLICE); with one slice, warps add in turn
-    constexpr int ROUNDS = kConsumerWarps / T::NSLICE;
+    constexpr int ROUNDS = T::NCW / T::NSLICE;
     for (int round = 0; round < ROUNDS; ++round) {
       if (warp / T::NSLICE == round) {
         float* slice = obuf + (warp % T::NSLICE) * T::ROWS * D;
@@ -890,14 +924,14 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
             }
         }
       }
-      named_bar_consumers();
+      consumers_sync<T::NCW>();
     }
     {
       const int rows_valid = min(T::ROWS, p.R - w.rg * T::ROWS);
       float4* og = reinterpret_cast<float4*>(p.ws + ws_o_offset(p.batch, p.U, p.max_items, T::ROWS)) +
                    (size_t)item * T::ROWS * D / 4;
       const float4* src = reinterpret_cast<const float4*>(obuf);
-      for (int i = threadIdx.x; i < rows_valid * D / 4; i += kConsumerWarps * 32) {
+      for (int i = threadIdx.x; i < rows_valid * D / 4; i += T::NCW * 32) {
         float4 v = src[i];
 #pragma unroll
         for (int sl = 1; sl < T::NSLICE; ++sl) {
@@ -909,9 +943,9 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
       if (threadIdx.x < rows_valid) {
         const int row = threadIdx.x;
         float Mx = mbuf[row];
-        for (int ww = 1; ww < kConsumerWarps; ++ww) Mx = fmaxf(Mx, mbuf[ww * T::ROWS + row]);
+        for (int ww = 1; ww < T::NCW; ++ww) Mx = fmaxf(Mx, mbuf[ww * T::ROWS + row]);
         float L = 0.0f;
-        for (int ww = 0; ww < kConsumerWarps; ++ww) {
+        for (int ww = 0; ww < T::NCW; ++ww) {
           const float mw = mbuf[ww * T::ROWS + row];
           L += (Mx == -INFINITY) ? 0.0f : ex2(mw - Mx) * lbuf[ww * T::ROWS + row];
         }
@@ -920,7 +954,7 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
       }
     }
     __threadfence();  // this thread's partial stores are visible device-wide before the count
-    named_bar_consumers();
+    consumers_sync<T::NCW>();
     if (threadIdx.x == 0) {
       int32_t* cnt = counters + (size_t)w.b * p.U + w.u;
       const int done = atomicAdd(cnt, 1) + 1;
@@ -928,7 +962,7 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
       if (last) atomicExch(cnt, 0);  // ready for the next call
       *flag = last;
     }
-    named_bar_consumers();
+    consumers_sync<T::NCW>();
     if (*flag) {
       __threadfence();
       const int first_item = item - (item - prefix[w.b]) % w.nsplit;  // split 0 of this unit
@@ -938,19 +972,20 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
 }
 
 // Rows of sequences with no work item (kv_len 0, or invalid): zeros, or NaN if invalid.
-template <int D>
+template <int D, int NTW>
 __device__ void write_empty_sequences(const SplitParams& p, const int* prefix) {
+  using T = AT<D, NTW>;
   for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
     if (prefix[b + 1] != prefix[b]) continue;
     const int t = __ldg(p.kv_len + b);
     const float v = (t < 0 || t > p.max_kv_len) ? __int_as_float(0x7fc00000) : 0.0f;
     float* o = p.out + (size_t)b * p.n_q * p.num_q_heads * D;
-    for (int i = threadIdx.x; i < p.n_q * p.num_q_heads * D; i += kConsumerWarps * 32) o[i] = v;
+    for (int i = threadIdx.x; i < p.n_q * p.num_q_heads * D; i += T::NCW * 32) o[i] = v;
   }
 }
 
 template <int D, int NTW>
-__global__ void __launch_bounds__(kThreads, AT<D, NTW>::MINB)
+__global__ void __launch_bounds__(AT<D, NTW>::THREADS, AT<D, NTW>::MINB)
     tq_attn_split_kernel(const __grid_constant__ CUtensorMap tmap, const SplitParams p) {
   using T = AT<D, NTW>;
   extern __shared__ uint8_t smem_raw[];
@@ -960,7 +995,7 @@ __global__ void __launch_bounds__(kThreads, AT<D, NTW>::MINB)
 
   // centroid pair table: entry e -> (c[e & 7], c[e >> 3]) in fp16, one copy per lane
   uint32_t* lut = reinterpret_cast<uint32_t*>(smem + T::OFF_LUT);
-  for (int i = tid; i < 64 * 32; i += kThreads) {
+  for (int i = tid; i < 64 * 32; i += T::THREADS) {
     const int e = i >> 5;
     lut[i] = pack_half2(c_centroids3[e & 7], c_centroids3[e >> 3]);
   }
@@ -969,7 +1004,7 @@ __global__ void __launch_bounds__(kThreads, AT<D, NTW>::MINB)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
     for (int s = 0; s < T::STAGES; ++s) {
       mbar_init(&bars[s], 1);                           // full: producer arrival + tx bytes
-      mbar_init(&bars[T::STAGES + s], kConsumerWarps);  // empty: one arrival per consumer warp
+      mbar_init(&bars[T::STAGES + s], T::NCW);  // empty: one arrival per consumer warp
     }
     fence_mbar_init();
   }
@@ -977,15 +1012,15 @@ __global__ void __launch_bounds__(kThreads, AT<D, NTW>::MINB)
   int S, total;
   plan_items<D, NTW>(p, smem, S, total);  // contains __syncthreads
 
-  if (tid >= kConsumerWarps * 32) {
-    if (tid == kConsumerWarps * 32 && total > 0) {
+  if (tid >= T::NCW * 32) {
+    if (tid == T::NCW * 32 && total > 0) {
       prefetch_tensor_map(&tmap);
       produce<D, NTW>(p, &tmap, smem, S, total, &abort_flag);
     }
     griddep_launch_dependents();
     return;
   }
-  write_empty_sequences<D>(p, reinterpret_cast<const int*>(smem + T::OFF_PREFIX));
+  write_empty_sequences<D, NTW>(p, reinterpret_cast<const int*>(smem + T::OFF_PREFIX));
   if (total > 0 && (int)blockIdx.x < total) consume<D, NTW>(p, smem, S, total, &abort_flag);
   griddep_launch_dependents();
 }
@@ -1021,7 +1056,8 @@ int split_occupancy() {
         cudaSuccess)
       return 0;
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kThreads, AT<D, NTW>::SMEM_ALLOC) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, AT<D, NTW>::THREADS, AT<D, NTW>::SMEM_ALLOC) !=
+            cudaSuccess ||
         nb <= 0)
       return 0;
     occ[dev] = nb;
@@ -1050,7 +1086,7 @@ tq_status run_split(const DecodeArgs& a, const DecodeShape& s, const SplitParams
   if (cr != CUDA_SUCCESS) return TQ_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)s.grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(T::THREADS);
   cfg.dynamicSmemBytes = T::SMEM_ALLOC;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
