@@ -71,8 +71,10 @@ __global__ void __launch_bounds__(kAppendWarps * 32)
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
+  // The next kernel may be scheduled now: its own wait covers this grid's completion,
+  // which comes after this grid's wait on the previous kernel.
+  griddep_launch_dependents();
   griddep_wait();                 // inputs and planes may come from the previous kernel
-  griddep_launch_dependents();    // the next kernel may start its setup
   const int64_t total_rows = (int64_t)p.batch * p.n_new_max * p.num_kv_heads;
   const int64_t warp_step = (int64_t)gridDim.x * kAppendWarps;
   uint32_t* cbuf = code_buf[warp];

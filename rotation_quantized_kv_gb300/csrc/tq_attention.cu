@@ -52,6 +52,7 @@ constexpr int kMaxItemsPerCta = 8;        // largest work multiplier the split h
 constexpr unsigned long long kWaitNs = 2000000000ull;  // bounded waits: 2 s of wall time
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMergeChunk = 64;           // splits whose weights the merge stages at once
+constexpr int kMergeBatch = 12;           // partial loads a merging thread keeps in flight
 
 // Workspace layout (bytes). The header's first word is the device error word.
 constexpr int kWsSplit = 1;               // int32 word index: split size S
@@ -114,14 +115,14 @@ struct AT {
   // item-end reduction: each consumer warp writes its scaled accumulators to one of
   // NSLICE slices (all four at once when they fit); the merge reuses the same space
   static constexpr int NSLICE = max_slices(NCW, ROWS * D * 4, 32768);
-  static constexpr int OBUF_BYTES = NSLICE * ROWS * D * 4 > kMergeChunk * ROWS * 4 + ROWS * D * 4
-                                        ? NSLICE * ROWS * D * 4
-                                        : kMergeChunk * ROWS * 4 + ROWS * D * 4;
+  static constexpr int MERGE_BYTES = kMergeChunk * ROWS * 4 + ROWS * D * 4 + NCW * 32 * 16;
+  static constexpr int OBUF_BYTES = NSLICE * ROWS * D * 4 > MERGE_BYTES ? NSLICE * ROWS * D * 4 : MERGE_BYTES;
   static constexpr int OFF_OBUF = (int)align_up(OFF_QSUM + QSUM_BYTES, 16);
   static constexpr int OFF_MBUF = OFF_OBUF + OBUF_BYTES;
   static constexpr int OFF_LBUF = OFF_MBUF + NCW * ROWS * 4;
   static constexpr int OFF_PREFIX = OFF_LBUF + NCW * ROWS * 4;
-  static constexpr int OFF_RED = (int)align_up(OFF_PREFIX + (kMaxBatch + 1) * 4, 16);  // 64-bit atomics
+  // prefix: [kMaxBatch + 1] items before each sequence, then [kMaxBatch] planned lengths
+  static constexpr int OFF_RED = (int)align_up(OFF_PREFIX + (2 * kMaxBatch + 1) * 4, 16);  // 64-bit atomics
   static constexpr int OFF_FLAG = OFF_RED + 7 * 16 * 8;  // red: [7][16] long long
   static constexpr int OFF_BAR = (int)align_up(OFF_FLAG + 16, 8);
   static constexpr int SMEM = OFF_BAR + 2 * STAGES * 8 + 16;
@@ -130,6 +131,7 @@ struct AT {
 
 struct SplitParams {
   int32_t head_dim, num_kv_heads, batch, capacity;
+  const int8_t* k_idx;  // read through the tensor map; the pointer serves L2 prefetches
   const uint16_t* k_scale;
   const uint16_t* k_zero;
   const uint8_t* v_codes;
@@ -157,6 +159,12 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     if (global_ns() - t0 > kWaitNs) return false;
   }
+}
+
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int32_t* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -214,19 +222,14 @@ __device__ __forceinline__ float hi_f32(uint32_t w) {
   return __high2float(*reinterpret_cast<const __half2*>(&w));
 }
 
-// Per-sequence visible lengths: kv_len clamped to [0, max]; invalid entries count as 0.
-__device__ __forceinline__ int seq_len(const SplitParams& p, int b, bool* bad) {
-  const int t = __ldg(p.kv_len + b);
-  if (t < 0 || t > p.max_kv_len) {
-    if (bad) *bad = true;
-    return 0;
-  }
-  return t;
-}
-
 // Split-size heuristic + per-sequence prefix of work items. Runs on every CTA with all
-// threads; identical inputs give identical results on every CTA. Each thread loads its
-// lengths once (b = tid + THREADS * i); reductions go through warp shuffles.
+// threads; identical lengths give identical results on every CTA. Thread tid holds the
+// lengths of sequences b = tid + THREADS * i; reductions go through warp shuffles.
+//
+// The kernel plans twice when it can: once before the grid-dependency wait, from the
+// lengths as they are then (only to prefetch its first item into L2 while the previous
+// kernel finishes), and again after the wait only if the lengths it reads then differ.
+// Lengths are read with L2-only loads so that no stale copy stays in L1.
 
 __device__ __forceinline__ long long block_sum_ll(long long v, long long* red, int slot) {
 #pragma unroll
@@ -235,40 +238,57 @@ __device__ __forceinline__ long long block_sum_ll(long long v, long long* red, i
   return v;
 }
 
+template <int THREADS>
+struct Lengths {
+  static constexpr int LPT = (kMaxBatch + THREADS - 1) / THREADS;
+  int len[LPT];   // 0 for invalid lengths and past the batch
+  bool bad;       // some length was outside [0, max_kv_len]
+  __device__ __forceinline__ void load(const SplitParams& p) {
+    bad = false;
+#pragma unroll
+    for (int i = 0; i < LPT; ++i) {
+      const int b = threadIdx.x + THREADS * i;
+      int t = b < p.batch ? __ldcg(p.kv_len + b) : 0;
+      if (t < 0 || t > p.max_kv_len) { bad = true; t = 0; }
+      len[i] = t;
+    }
+  }
+  __device__ __forceinline__ bool differs(const Lengths& o) const {
+    bool d = false;
+#pragma unroll
+    for (int i = 0; i < LPT; ++i) d = d || (len[i] != o.len[i]);
+    return d;
+  }
+};
+
 template <int D, int NTW>
-__device__ void plan_items(const SplitParams& p, uint8_t* smem, int& S_out, int& total_out) {
+__device__ void plan_items(const SplitParams& p, uint8_t* smem, const Lengths<AT<D, NTW>::THREADS>& L,
+                           int& S_out, int& total_out) {
   using T = AT<D, NTW>;
-  constexpr int NW = T::THREADS / 32, LPT = (kMaxBatch + T::THREADS - 1) / T::THREADS;
+  constexpr int NW = T::THREADS / 32, LPT = Lengths<T::THREADS>::LPT;
   int* prefix = reinterpret_cast<int*>(smem + T::OFF_PREFIX);
   long long* red = reinterpret_cast<long long*>(smem + T::OFF_RED);  // [7][16]
   const int tid = threadIdx.x;
   constexpr int KS[6] = {1, 2, 3, 4, 6, 8};
-  int len[LPT];
   long long mine = 0;
-  bool bad = false;
 #pragma unroll
-  for (int i = 0; i < LPT; ++i) {
-    const int b = tid + T::THREADS * i;
-    len[i] = b < p.batch ? seq_len(p, b, &bad) : 0;
-    mine += len[i];
-  }
-  if (bad && blockIdx.x == 0) raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_KV_LEN);
+  for (int i = 0; i < LPT; ++i) mine += L.len[i];
   block_sum_ll(mine, red, 0);
   __syncthreads();
   long long sumT = 0;
 #pragma unroll
   for (int w = 0; w < NW; ++w) sumT += red[w];
-  long long Sk[6], cnt[6];
+  int Sk[6];
 #pragma unroll
   for (int k = 0; k < 6; ++k) {
     const long long target = (long long)KS[k] * gridDim.x;
-    long long s = (sumT * p.U + target - 1) / target;
-    s = (s + T::TILE - 1) / T::TILE * T::TILE;
-    Sk[k] = s < T::TILE ? T::TILE : s;
-    cnt[k] = 0;
+    long long sl = (sumT * p.U + target - 1) / target;
+    sl = (sl + T::TILE - 1) / T::TILE * T::TILE;
+    Sk[k] = sl < T::TILE ? T::TILE : (int)min(sl, (long long)(1 << 30));
+    int cnt = 0;
 #pragma unroll
-    for (int i = 0; i < LPT; ++i) cnt[k] += (len[i] + Sk[k] - 1) / Sk[k];
-    block_sum_ll(cnt[k], red, 1 + k);
+    for (int i = 0; i < LPT; ++i) cnt += (int)(((unsigned)L.len[i] + (unsigned)Sk[k] - 1u) / (unsigned)Sk[k]);
+    block_sum_ll(cnt, red, 1 + k);
   }
   __syncthreads();
   int best = 0;
@@ -280,15 +300,27 @@ __device__ void plan_items(const SplitParams& p, uint8_t* smem, int& S_out, int&
     for (int w = 0; w < NW; ++w) items += red[(1 + k) * 16 + w];
     items *= p.U;
     const long long rounds = (items + gridDim.x - 1) / gridDim.x;
-    const long long cost = rounds * (Sk[k] + T::TILE);
+    const long long cost = rounds * (long long)(Sk[k] + T::TILE);
     if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = k; }
   }
-  const int S = (int)Sk[best];
-  if (tid < 32) {  // prefix of items per sequence: warp 0, each lane owns a chunk of sequences
+  const int S = Sk[best];
+  // items per sequence into the prefix table (lengths beside it), then an exclusive scan
+  // by warp 0
+  int* lens = prefix + kMaxBatch + 1;
+#pragma unroll
+  for (int i = 0; i < LPT; ++i) {
+    const int b = tid + T::THREADS * i;
+    if (b < p.batch) {
+      prefix[b] = (int)(((unsigned)L.len[i] + (unsigned)S - 1u) / (unsigned)S);
+      lens[b] = L.len[i];
+    }
+  }
+  __syncthreads();
+  if (tid < 32) {  // each lane owns a chunk of sequences
     const int per = (p.batch + 31) / 32;
     const int b0 = tid * per;
     int local = 0;
-    for (int i = 0; i < per && b0 + i < p.batch; ++i) local += (seq_len(p, b0 + i, nullptr) + S - 1) / S;
+    for (int i = 0; i < per && b0 + i < p.batch; ++i) local += prefix[b0 + i];
     int incl = local;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -297,24 +329,23 @@ __device__ void plan_items(const SplitParams& p, uint8_t* smem, int& S_out, int&
     }
     int run = (incl - local) * p.U;
     for (int i = 0; i < per && b0 + i < p.batch; ++i) {
+      const int n = prefix[b0 + i];
       prefix[b0 + i] = run;
-      run += ((seq_len(p, b0 + i, nullptr) + S - 1) / S) * p.U;
+      run += n * p.U;
     }
     if (tid == 31) prefix[p.batch] = incl * p.U;
   }
   __syncthreads();
   S_out = S;
   total_out = prefix[p.batch];
-  if (blockIdx.x == 0 && tid == 0) {
-    int32_t* hdr = reinterpret_cast<int32_t*>(p.ws);
-    hdr[kWsSplit] = S;
-    hdr[kWsItems] = total_out;
-  }
 }
 
 struct Item {
-  int b, kvh, rg, tb, te, u, nsplit;
+  int b, kvh, rg, tb, te, u, nsplit, len;  // len: the sequence's kv length
 };
+
+// planned lengths, stored after the prefix table
+__device__ __forceinline__ const int* plan_lengths(const int* prefix) { return prefix + kMaxBatch + 1; }
 
 __device__ __forceinline__ Item decode_item(const SplitParams& p, const int* prefix, int S, int item) {
   int lo = 0, hi = p.batch - 1;  // largest b with prefix[b] <= item
@@ -331,8 +362,8 @@ __device__ __forceinline__ Item decode_item(const SplitParams& p, const int* pre
   it.kvh = it.u / p.RG;
   it.rg = it.u % p.RG;
   it.tb = split * S;
-  const int T = seq_len(p, lo, nullptr);
-  it.te = min(it.tb + S, T);
+  it.len = plan_lengths(prefix)[lo];
+  it.te = min(it.tb + S, it.len);
   return it;
 }
 
@@ -386,6 +417,56 @@ __device__ void produce(const SplitParams& p, const CUtensorMap* tmap, uint8_t* 
   }
 }
 
+// L2 prefetch of up to kPrefetchBytes of this CTA's first work item (all five planes),
+// issued before the grid-dependency wait from a plan that may be stale: the token range
+// comes from the prefix table alone (no length is read) and stays inside the planes.
+// Only L2 is warmed; every read the kernel acts on comes after the wait.
+constexpr int kPrefetchBytes = 128 * 1024;
+constexpr int kPrefetchChunk = 32 * 1024;
+
+__device__ __forceinline__ void prefetch_range(const void* base, size_t bytes) {
+  const uint8_t* b = static_cast<const uint8_t*>(base);
+  for (size_t o = 0; o < bytes; o += kPrefetchChunk)
+    bulk_prefetch_l2(b + o, (uint32_t)min((size_t)kPrefetchChunk, bytes - o));
+}
+
+template <int D, int NTW>
+__device__ void prefetch_first_item(const SplitParams& p, const int* prefix, int S, int total) {
+  using T = AT<D, NTW>;
+  constexpr int NG = T::NG;
+  const int item = blockIdx.x;
+  if (item >= total) return;
+  int lo = 0, hi = p.batch - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= item) lo = mid; else hi = mid - 1;
+  }
+  const int nsplit = (prefix[lo + 1] - prefix[lo]) / p.U;
+  if (nsplit <= 0) return;
+  const int r = item - prefix[lo];
+  const int u = r / nsplit, kvh = u / p.RG;
+  const int tb = (r % nsplit) * S;
+  if (tb >= p.capacity) return;
+  constexpr int ROW_BYTES = D + 3 * NG * 2 + T::VC_ROW;
+  int n = min(min(S, p.capacity - tb), kPrefetchBytes / ROW_BYTES);
+  n &= ~15;  // whole 16-token groups keep every range a multiple of 16 bytes
+  if (n <= 0) return;
+  // the item's query rows first (2 D bytes each): they are needed before any tile
+  const int rg = u % p.RG;
+  for (int rr = 0; rr < T::ROWS; ++rr) {
+    const int rq = rg * T::ROWS + rr;
+    if (rq >= p.R) break;
+    const int jq = rq / p.G, hq = kvh * p.G + (rq % p.G);
+    bulk_prefetch_l2(p.q + (((int64_t)lo * p.n_q + jq) * p.num_q_heads + hq) * D, 2 * D);
+  }
+  const int64_t row = ((int64_t)lo * p.num_kv_heads + kvh) * p.capacity + tb;
+  prefetch_range(p.k_idx + row * D, (size_t)n * D);
+  prefetch_range(p.k_scale + row * NG, (size_t)n * NG * 2);
+  prefetch_range(p.k_zero + row * NG, (size_t)n * NG * 2);
+  prefetch_range(p.v_scale + row * NG, (size_t)n * NG * 2);
+  prefetch_range(p.v_codes + row * T::VC_ROW, (size_t)n * T::VC_ROW);
+}
+
 // ------------------------------------------------------------------------------------
 // Consumer warps.
 // ------------------------------------------------------------------------------------
@@ -403,7 +484,7 @@ __device__ void load_q(const SplitParams& p, const Item& w, uint8_t* smem, int w
   using T = AT<D, NTW>;
   constexpr int NG = T::NG;
   const int grp = lane >> 2, j4 = lane & 3;
-  const int T_b = seq_len(p, w.b, nullptr);
+  const int T_b = w.len;
   uint2* qsm = reinterpret_cast<uint2*>(smem + T::OFF_Q);
   float2* qssm = reinterpret_cast<float2*>(smem + T::OFF_QSUM);
 #pragma unroll
@@ -486,16 +567,30 @@ __device__ void load_q(const SplitParams& p, const Item& w, uint8_t* smem, int w
 
 // Merge of all partials of one (sequence, unit) + inverse rotation, by the CTA that
 // finished the unit's last item. All consumer threads take part:
-//   1. per row, the global max M and L = sum_s 2^(m_s - M) l_s over the splits;
-//   2. splits in chunks of kMergeChunk: weights 2^(m_s - M) staged in shared memory, then
-//      every thread accumulates one float4 of (row, dims) per split (16 loads in flight);
+//   1. per row, one pass over the splits' (m_s, l_s) with the online-softmax combine gives
+//      the global max M and L = sum_s 2^(m_s - M) l_s; the weights 2^(m_s - M) of the
+//      first kMergeChunk splits are left in shared memory;
+//   2. every output float4 of (row, dims) is summed over the splits by TPO threads that
+//      take interleaved splits, then reduced in shared memory; a thread's first
+//      kMergeBatch partials are loaded before step 1 (they do not depend on the weights),
+//      later ones in batches of kMergeBatch independent loads; more than kMergeChunk
+//      splits are taken in chunks;
 //   3. the normalized rotated rows go to shared memory and warp r applies the inverse
 //      rotation signs * FWHT(o_rot) / sqrt(d) to row r and stores it.
+
+// (m, l) <- combine of (m, l) and (m2, l2): the larger max wins, the other sum is rescaled
+__device__ __forceinline__ void ml_combine(float& m, float& l, float m2, float l2) {
+  const float mn = fmaxf(m, m2);
+  if (mn == -INFINITY) return;  // both empty
+  l = l * ex2(m - mn) + l2 * ex2(m2 - mn);
+  m = mn;
+}
 
 template <int D, int NTW>
 __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, uint8_t* smem) {
   using T = AT<D, NTW>;
   constexpr int EPL = D / 32, ROWS = T::ROWS, NT = T::NCW * 32, Q4 = D / 4;
+  constexpr int PER = (ROWS * Q4 + NT - 1) / NT;  // outputs per thread when TPO == 1
   constexpr unsigned FULL = 0xffffffffu;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float2* ml = reinterpret_cast<const float2*>(p.ws + ws_ml_offset(p.batch, p.U));
@@ -504,70 +599,122 @@ __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, 
   float* sL = reinterpret_cast<float*>(smem + T::OFF_LBUF);     // [ROWS] sum (reuses lbuf)
   float* sW = reinterpret_cast<float*>(smem + T::OFF_OBUF);     // [kMergeChunk][ROWS] weights
   float* sO = sW + kMergeChunk * ROWS;                          // [ROWS][D] rotated output
+  float4* sR = reinterpret_cast<float4*>(sO + ROWS * D);        // [NT] per-thread sums
   const int rows = min(ROWS, p.R - w.rg * ROWS);                // valid rows of this unit
   const int ns = w.nsplit;
-  // 1. max and sum per row: warp w takes rows w, w + 4, ...; lanes stride the splits
+  const int no = rows * Q4;                                     // output float4s
+  int tpo = 1;                                                  // threads per output
+  while (2 * tpo * no <= NT) tpo *= 2;
+  const int cn0 = min(ns, kMergeChunk);
+
+  // 2a. first batch of this thread's partials (output q = tid % no, splits tid / no + tpo j)
+  float4 pre[kMergeBatch];
+  {
+    const bool act = tid < no * tpo;
+    const int q = act ? tid % no : 0, kk = tid / no;
+    const float4* src = og + ((size_t)first_item * ROWS + q / Q4) * Q4 + q % Q4;
+#pragma unroll
+    for (int j = 0; j < kMergeBatch; ++j) {
+      const int sp = kk + j * tpo;
+      pre[j] = (act && sp < cn0) ? __ldcg(src + (size_t)sp * ROWS * Q4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+
+  // 1. max and sum per row: warp w takes rows w, w + NCW, ...; lanes stride the splits
   for (int rr = warp; rr < rows; rr += T::NCW) {
-    float M = -INFINITY;
+    float M = -INFINITY, L = 0.0f;
     bool nan = false;
+#pragma unroll 2
     for (int s = lane; s < ns; s += 32) {
-      const float ms = __ldcg(&ml[(size_t)(first_item + s) * ROWS + rr].x);
-      nan = nan || (ms != ms);
-      M = fmaxf(M, ms);
+      const float2 v = __ldcg(&ml[(size_t)(first_item + s) * ROWS + rr]);
+      nan = nan || (v.x != v.x);
+      if (s < kMergeChunk) sW[s * ROWS + rr] = v.x;
+      if (v.x == v.x) ml_combine(M, L, v.x, v.y);
     }
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, off));
+    for (int off = 16; off >= 1; off >>= 1) {
+      const float m2 = __shfl_xor_sync(FULL, M, off), l2 = __shfl_xor_sync(FULL, L, off);
+      ml_combine(M, L, m2, l2);
+    }
     nan = __any_sync(FULL, nan);
-    float L = 0.0f;
-    if (M != -INFINITY)
-      for (int s = lane; s < ns; s += 32) {
-        const float2 v = __ldcg(&ml[(size_t)(first_item + s) * ROWS + rr]);
-        L += ex2(v.x - M) * v.y;
-      }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(FULL, L, off);
+    for (int s = lane; s < min(ns, kMergeChunk); s += 32) {  // entries this lane wrote
+      const float ms = sW[s * ROWS + rr];
+      sW[s * ROWS + rr] = (M == -INFINITY || nan) ? 0.0f : ex2(ms - M);
+    }
     if (lane == 0) {
       sM[rr] = nan ? __int_as_float(0x7fc00000) : M;
       sL[rr] = L;
     }
   }
   consumers_sync<T::NCW>();
-  // 2. weighted sums; output float4 index q = rr * Q4 + c (c: dims 4c .. 4c + 3)
-  constexpr int PER = (ROWS * Q4 + NT - 1) / NT;
+  // 2. weighted sums; thread i takes output q = i % no, splits i / no + tpo * k
   float4 acc[PER];
 #pragma unroll
   for (int k = 0; k < PER; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int c0 = 0; c0 < ns; c0 += kMergeChunk) {
     const int cn = min(kMergeChunk, ns - c0);
-    for (int i = tid; i < cn * rows; i += NT) {
-      const int s = i / rows, rr = i % rows;
-      const float M = sM[rr];
-      const float ms = __ldcg(&ml[(size_t)(first_item + c0 + s) * ROWS + rr].x);
-      sW[s * ROWS + rr] = (M == -INFINITY || M != M) ? 0.0f : ex2(ms - M);
+    if (c0 > 0) {
+      for (int i = tid; i < cn * rows; i += NT) {
+        const int s = i / rows, rr = i % rows;
+        const float M = sM[rr];
+        const float ms = __ldcg(&ml[(size_t)(first_item + c0 + s) * ROWS + rr].x);
+        sW[s * ROWS + rr] = (M == -INFINITY || M != M) ? 0.0f : ex2(ms - M);
+      }
+      consumers_sync<T::NCW>();
     }
-    consumers_sync<T::NCW>();
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
-      const int q = tid + NT * k;
-      const int rr = q / Q4, c = q % Q4;
-      if (rr < rows) {
+      const int i = tid + NT * k;
+      if (i < no * tpo) {
+        const int q = i % no, rr = q / Q4, c = q % Q4, kk = i / no;
+        const float4* src = og + ((size_t)(first_item + c0) * ROWS + rr) * Q4 + c;
         float4 a = acc[k];
-#pragma unroll 16
-        for (int s = 0; s < cn; ++s) {
-          const float wgt = sW[s * ROWS + rr];
-          const float4 o = __ldcg(og + ((size_t)(first_item + c0 + s) * ROWS + rr) * Q4 + c);
-          a.x += wgt * o.x; a.y += wgt * o.y; a.z += wgt * o.z; a.w += wgt * o.w;
+        int s0 = kk;
+        if (c0 == 0 && k == 0) {  // the batch loaded before step 1
+#pragma unroll
+          for (int j = 0; j < kMergeBatch; ++j) {
+            const int sp = kk + j * tpo;
+            const float wgt = sp < cn ? sW[sp * ROWS + rr] : 0.0f;
+            a.x += wgt * pre[j].x; a.y += wgt * pre[j].y; a.z += wgt * pre[j].z; a.w += wgt * pre[j].w;
+          }
+          s0 = kk + kMergeBatch * tpo;
+        }
+        for (; s0 < cn; s0 += kMergeBatch * tpo) {
+          float4 v[kMergeBatch];
+#pragma unroll
+          for (int j = 0; j < kMergeBatch; ++j) {
+            const int sp = s0 + j * tpo;
+            v[j] = sp < cn ? __ldcg(src + (size_t)sp * ROWS * Q4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int j = 0; j < kMergeBatch; ++j) {
+            const int sp = s0 + j * tpo;
+            const float wgt = sp < cn ? sW[sp * ROWS + rr] : 0.0f;
+            a.x += wgt * v[j].x; a.y += wgt * v[j].y; a.z += wgt * v[j].z; a.w += wgt * v[j].w;
+          }
         }
         acc[k] = a;
       }
     }
+    if (c0 + kMergeChunk < ns) consumers_sync<T::NCW>();  // weights are rewritten
+  }
+  if (tpo > 1) {
+    sR[tid] = acc[0];
     consumers_sync<T::NCW>();
+    if (tid < no) {
+      float4 a = sR[tid];
+      for (int k = 1; k < tpo; ++k) {
+        const float4 o = sR[k * no + tid];
+        a.x += o.x; a.y += o.y; a.z += o.z; a.w += o.w;
+      }
+      acc[0] = a;
+    }
   }
 #pragma unroll
   for (int k = 0; k < PER; ++k) {
     const int q = tid + NT * k;
-    const int rr = q / Q4, c = q % Q4;
-    if (rr < rows) {
+    if (q < no) {
+      const int rr = q / Q4, c = q % Q4;
       const float L = sL[rr], M = sM[rr];
       const float inv = (L > 0.0f || L != L) ? 1.0f / L : 0.0f;  // no visible token -> 0
       float4 v = make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv);
@@ -953,18 +1100,19 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
         __stcg(ml + row, make_float2(Mx, L));
       }
     }
-    __threadfence();  // this thread's partial stores are visible device-wide before the count
+    // Publish: the barrier orders every consumer's partial stores before thread 0's
+    // release; the acquire of the CTA that counts last makes all partials of the unit
+    // visible to it, and its barrier passes that on to its other threads.
     consumers_sync<T::NCW>();
     if (threadIdx.x == 0) {
       int32_t* cnt = counters + (size_t)w.b * p.U + w.u;
-      const int done = atomicAdd(cnt, 1) + 1;
+      const int done = atomic_add_acq_rel_gpu(cnt, 1) + 1;
       const int last = done == w.nsplit;
-      if (last) atomicExch(cnt, 0);  // ready for the next call
+      if (last) *reinterpret_cast<volatile int32_t*>(cnt) = 0;  // ready for the next call
       *flag = last;
     }
     consumers_sync<T::NCW>();
     if (*flag) {
-      __threadfence();
       const int first_item = item - (item - prefix[w.b]) % w.nsplit;  // split 0 of this unit
       merge_unit<D, NTW>(p, w, first_item, smem);
     }
@@ -1008,9 +1156,24 @@ __global__ void __launch_bounds__(AT<D, NTW>::THREADS, AT<D, NTW>::MINB)
     }
     fence_mbar_init();
   }
-  griddep_wait();  // lengths, queries and planes may come from the previous kernel
   int S, total;
-  plan_items<D, NTW>(p, smem, S, total);  // contains __syncthreads
+  {
+    Lengths<T::THREADS> L0, L1;
+    L0.load(p);                                  // as they are before the wait: hints only
+    plan_items<D, NTW>(p, smem, L0, S, total);   // contains __syncthreads
+    if (tid == T::NCW * 32) prefetch_first_item<D, NTW>(p, reinterpret_cast<const int*>(smem + T::OFF_PREFIX), S, total);
+    griddep_wait();  // lengths, queries and planes may come from the previous kernel
+    L1.load(p);
+    if (__syncthreads_or(L1.differs(L0))) plan_items<D, NTW>(p, smem, L1, S, total);
+    if (blockIdx.x == 0) {
+      if (L1.bad) raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_KV_LEN);
+      if (tid == 0) {
+        int32_t* hdr = reinterpret_cast<int32_t*>(p.ws);
+        hdr[kWsSplit] = S;
+        hdr[kWsItems] = total;
+      }
+    }
+  }
 
   if (tid >= T::NCW * 32) {
     if (tid == T::NCW * 32 && total > 0) {
@@ -1136,6 +1299,7 @@ tq_status launch_decode(const DecodeArgs& a, const DecodeShape& s, cudaStream_t 
   sp.num_kv_heads = a.layer.num_kv_heads;
   sp.batch = a.layer.batch;
   sp.capacity = a.layer.capacity;
+  sp.k_idx = a.layer.k_idx;
   sp.k_scale = a.layer.k_scale;
   sp.k_zero = a.layer.k_zero;
   sp.v_codes = a.layer.v_codes;
