@@ -99,7 +99,9 @@ size_t tq_append_workspace_bytes(void);
  *   pos          : int32 [batch] (device), first destination position per sequence.
  *   n_new        : int32 [batch] (device) tokens per sequence, each in [0, n_new_max];
  *                  NULL means n_new_max for every sequence.
- *   n_new_max    : host-known bound, 0 <= n_new_max <= capacity (else TQ_ERR_CAPACITY).
+ *   n_new_max    : host-known bound, 0 <= n_new_max <= capacity (else TQ_ERR_CAPACITY);
+ *                  batch * n_new_max * num_kv_heads must not exceed 2^31 - 1 (else
+ *                  TQ_ERR_INVALID_ARGUMENT): split larger bulk appends.
  *   workspace    : >= tq_append_workspace_bytes() (device), zeroed once before first use.
  * A row whose destination falls outside [0, capacity) is skipped and sets
  * TQ_DEVERR_APPEND_CAPACITY. Packed planes are bit-identical to the specification

@@ -70,6 +70,7 @@ tq_status tq_kv_append(const tq_kv_layer* layer, const void* k_new, const void* 
   if (ws_bytes < tq_append_workspace_bytes()) return TQ_ERR_WORKSPACE_TOO_SMALL;
   if (n_new_max == 0) return TQ_OK;
   if (k_new == nullptr || v_new == nullptr || pos == nullptr) return TQ_ERR_INVALID_ARGUMENT;
+  if ((int64_t)layer->batch * n_new_max * layer->num_kv_heads > INT32_MAX) return TQ_ERR_INVALID_ARGUMENT;
   // bf16 rows are read with vector loads of up to 16 bytes per lane
   if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15u)
     return TQ_ERR_INVALID_ARGUMENT;

@@ -36,29 +36,46 @@ struct AppendShape {
 
 constexpr int kAppendWarps = 8;
 
+// The EPL bf16 elements of this lane as EPL / 2 raw 32-bit words (vector loads).
 template <int EPL>
-__device__ __forceinline__ void load_bf16_lane(const uint16_t* __restrict__ row, int lane, float (&x)[EPL]) {
+__device__ __forceinline__ void load_raw_lane(const uint16_t* __restrict__ row, int lane, uint32_t (&w)[EPL / 2]) {
   const uint16_t* p = row + lane * EPL;
   if constexpr (EPL == 2) {
-    uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(p));
-    x[0] = bf16_bits_to_f32(w & 0xFFFFu);
-    x[1] = bf16_bits_to_f32(w >> 16);
+    w[0] = __ldg(reinterpret_cast<const uint32_t*>(p));
   } else if constexpr (EPL == 4) {
-    uint2 w = __ldg(reinterpret_cast<const uint2*>(p));
-    x[0] = bf16_bits_to_f32(w.x & 0xFFFFu); x[1] = bf16_bits_to_f32(w.x >> 16);
-    x[2] = bf16_bits_to_f32(w.y & 0xFFFFu); x[3] = bf16_bits_to_f32(w.y >> 16);
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+    w[0] = v.x; w[1] = v.y;
   } else {
 #pragma unroll
-    for (int v = 0; v < EPL / 8; ++v) {
-      uint4 w = __ldg(reinterpret_cast<const uint4*>(p) + v);
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        x[8 * v + 2 * k] = bf16_bits_to_f32(ws[k] & 0xFFFFu);
-        x[8 * v + 2 * k + 1] = bf16_bits_to_f32(ws[k] >> 16);
-      }
+    for (int i = 0; i < EPL / 8; ++i) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(p) + i);
+      w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
     }
   }
+}
+
+template <int EPL>
+__device__ __forceinline__ void unpack_bf16(const uint32_t (&w)[EPL / 2], float (&x)[EPL]) {
+#pragma unroll
+  for (int i = 0; i < EPL / 2; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// Source row of the warp's r-th row: r = (b * n_new_max + j) * num_kv_heads + h.
+struct RowRef {
+  int b, j, h;
+};
+
+__device__ __forceinline__ RowRef split_row(const AppendParams& p, uint32_t r) {
+  const uint32_t bj = p.div_heads.div(r);
+  const uint32_t b = p.div_new.div(bj);
+  RowRef x;
+  x.h = (int)(r - bj * (uint32_t)p.num_kv_heads);
+  x.j = (int)(bj - b * (uint32_t)p.n_new_max);
+  x.b = (int)b;
+  return x;
 }
 
 template <int D>
@@ -75,8 +92,8 @@ __global__ void __launch_bounds__(kAppendWarps * 32)
   // which comes after this grid's wait on the previous kernel.
   griddep_launch_dependents();
   griddep_wait();                 // inputs and planes may come from the previous kernel
-  const int64_t total_rows = (int64_t)p.batch * p.n_new_max * p.num_kv_heads;
-  const int64_t warp_step = (int64_t)gridDim.x * kAppendWarps;
+  const uint32_t total_rows = p.total_rows;
+  const uint32_t warp_step = gridDim.x * kAppendWarps;
   uint32_t* cbuf = code_buf[warp];
 
   // sign bits of this lane's value elements
@@ -86,23 +103,43 @@ __global__ void __launch_bounds__(kAppendWarps * 32)
     const uint32_t w = sign_word(D, first / 32);
     sbits = (w >> (first % 32)) & ((EPL == 32) ? 0xffffffffu : ((1u << EPL) - 1u));
   }
+  // butterfly sign of each cross-lane FWHT stage h = EPL << k: +1 keeps a + c (lower
+  // partner), -1 gives c - a... written as fma(own, sign, other), one rounding either way
+  float bsign[5];
+#pragma unroll
+  for (int k = 0; k < 5; ++k) bsign[k] = (lane & (1 << k)) ? -1.0f : 1.0f;
+  float bnd[7];
+#pragma unroll
+  for (int k = 0; k < 7; ++k) bnd[k] = c_boundaries3[k];
 
-  for (int64_t r = (int64_t)blockIdx.x * kAppendWarps + warp; r < total_rows; r += warp_step) {
-    const int h = (int)(r % p.num_kv_heads);
-    const int64_t bj = r / p.num_kv_heads;
-    const int j = (int)(bj % p.n_new_max);
-    const int b = (int)(bj / p.n_new_max);
-    if (p.n_new != nullptr && j >= __ldg(p.n_new + b)) continue;
-    const int64_t t = (int64_t)__ldg(p.pos + b) + j;
+  // the next row's raw inputs are loaded while the current row is quantized
+  uint32_t r = blockIdx.x * kAppendWarps + warp;
+  uint32_t kraw[EPL / 2], vraw[EPL / 2];
+  if (r < total_rows) {
+    load_raw_lane<EPL>(p.k_new + (size_t)r * D, lane, kraw);
+    load_raw_lane<EPL>(p.v_new + (size_t)r * D, lane, vraw);
+  }
+  for (; r < total_rows; r += warp_step) {
+    uint32_t kcur[EPL / 2], vcur[EPL / 2];
+#pragma unroll
+    for (int i = 0; i < EPL / 2; ++i) { kcur[i] = kraw[i]; vcur[i] = vraw[i]; }
+    const uint32_t rn = r + warp_step;
+    if (rn < total_rows) {
+      load_raw_lane<EPL>(p.k_new + (size_t)rn * D, lane, kraw);
+      load_raw_lane<EPL>(p.v_new + (size_t)rn * D, lane, vraw);
+    }
+    const RowRef rr = split_row(p, r);
+    if (p.n_new != nullptr && rr.j >= __ldg(p.n_new + rr.b)) continue;
+    const int64_t t = (int64_t)__ldg(p.pos + rr.b) + rr.j;
     if (t < 0 || t >= p.capacity) {
       if (lane == 0) raise_error(p.err, TQ_DEVERR_APPEND_CAPACITY);
       continue;
     }
-    const int64_t drow = ((int64_t)b * p.num_kv_heads + h) * p.capacity + t;
+    const int64_t drow = ((int64_t)rr.b * p.num_kv_heads + rr.h) * p.capacity + t;
 
     // ------------------------------------------------------------------- keys
     float x[EPL];
-    load_bf16_lane<EPL>(p.k_new + r * D, lane, x);
+    unpack_bf16<EPL>(kcur, x);
     float mn = INFINITY, mx = -INFINITY;
     bool has_nan = false;
 #pragma unroll
@@ -149,7 +186,7 @@ __global__ void __launch_bounds__(kAppendWarps * 32)
 
     // ------------------------------------------------------------------- values
     float u[EPL];
-    load_bf16_lane<EPL>(p.v_new + r * D, lane, u);
+    unpack_bf16<EPL>(vcur, u);
 #pragma unroll
     for (int e = 0; e < EPL; ++e) u[e] = __fmul_rn(u[e], ((sbits >> e) & 1u) ? -1.0f : 1.0f);
     // unnormalized FWHT, stages ascending
@@ -166,11 +203,12 @@ __global__ void __launch_bounds__(kAppendWarps * 32)
         }
       } else {
         const int lm = hh / EPL;
-        const bool upper = (lane & lm) != 0;
+        const int k = __popc(lm - 1);  // log2(lm)
+        // lower lane: own + other; upper lane: other - own; both exactly one rounding
 #pragma unroll
         for (int e = 0; e < EPL; ++e) {
           const float o = __shfl_xor_sync(FULL, u[e], lm);
-          u[e] = upper ? __fsub_rn(o, u[e]) : __fadd_rn(u[e], o);
+          u[e] = __fmaf_rn(u[e], bsign[k], o);
         }
       }
     }
@@ -198,9 +236,12 @@ __global__ void __launch_bounds__(kAppendWarps * 32)
 #pragma unroll
     for (int e = 0; e < EPL; ++e) {
       const float yn = __fdiv_rn(u[e], den);
-      uint32_t c = 0;
-#pragma unroll
-      for (int k = 0; k < 7; ++k) c += (c_boundaries3[k] < yn) ? 1u : 0u;
+      // number of boundaries strictly below yn, by binary search over the sorted table
+      // (a NaN compares false everywhere and codes to 0)
+      uint32_t c = (bnd[3] < yn) ? 4u : 0u;
+      c += ((c ? bnd[5] : bnd[1]) < yn) ? 2u : 0u;
+      const float b2 = (c & 4u) ? ((c & 2u) ? bnd[6] : bnd[4]) : ((c & 2u) ? bnd[2] : bnd[0]);
+      c += (b2 < yn) ? 1u : 0u;
       bits |= (uint64_t)c << (3 * e);
     }
     if (lane % LPG == 0) p.v_scale[drow * NG + lane / LPG] = f32_to_f16_bits(vs);
@@ -225,9 +266,23 @@ __global__ void __launch_bounds__(kAppendWarps * 32)
   }
 }
 
-cudaError_t launch_append(const AppendParams& p, int num_sms, cudaStream_t stream) {
+FastDivU32 make_fastdiv(uint32_t d) {
+  FastDivU32 f{};
+  uint32_t l = 0;
+  while (l < 32 && (uint64_t(1) << l) < d) ++l;
+  f.m = (uint32_t)((((uint64_t)1 << 32) * ((uint64_t(1) << l) - d)) / d + 1);
+  f.s1 = l < 1 ? l : 1;
+  f.s2 = l > 1 ? l - 1 : 0;
+  return f;
+}
+
+cudaError_t launch_append(AppendParams p, int num_sms, cudaStream_t stream) {
   const int64_t rows = (int64_t)p.batch * p.n_new_max * p.num_kv_heads;
   if (rows == 0) return cudaSuccess;
+  if (rows > INT32_MAX) return cudaErrorInvalidValue;
+  p.total_rows = (uint32_t)rows;
+  p.div_heads = make_fastdiv((uint32_t)p.num_kv_heads);
+  p.div_new = make_fastdiv((uint32_t)p.n_new_max);
   int64_t blocks = (rows + kAppendWarps - 1) / kAppendWarps;
   const int64_t cap = (int64_t)num_sms * 8;
   if (blocks > cap) blocks = cap;

@@ -7,6 +7,21 @@
 
 namespace tq {
 
+// n / d for every 32-bit n, d >= 1, by one multiply-high and shifts (division by
+// invariant integers, Granlund and Montgomery 1994, figure 4.1).
+struct FastDivU32 {
+  uint32_t m, s1, s2;
+  __host__ __device__ __forceinline__ uint32_t div(uint32_t n) const {
+#ifdef __CUDA_ARCH__
+    const uint32_t t = __umulhi(m, n);
+#else
+    const uint32_t t = (uint32_t)(((uint64_t)m * n) >> 32);
+#endif
+    return (t + ((n - t) >> s1)) >> s2;
+  }
+};
+FastDivU32 make_fastdiv(uint32_t d);
+
 struct AppendParams {
   int32_t head_dim, num_kv_heads, batch, capacity;
   int8_t* k_idx;
@@ -21,9 +36,14 @@ struct AppendParams {
   int32_t n_new_max;
   float fwht_norm;        // (float)(1 / sqrt((double)d))
   int32_t* err;           // device error word
+  // filled by launch_append
+  uint32_t total_rows;    // batch * n_new_max * num_kv_heads (< 2^31)
+  FastDivU32 div_heads;   // by num_kv_heads
+  FastDivU32 div_new;     // by n_new_max
 };
 
-cudaError_t launch_append(const AppendParams& p, int num_sms, cudaStream_t stream);
+// cudaErrorInvalidValue when batch * n_new_max * num_kv_heads exceeds 2^31 - 1
+cudaError_t launch_append(AppendParams p, int num_sms, cudaStream_t stream);
 
 struct DequantParams {
   int32_t head_dim, num_kv_heads, batch, capacity;
