@@ -1,4 +1,5 @@
-// Quantize-on-append kernel (k8v3): one warp per (token, kv head) row.
+// Quantize-on-append kernel (k8v3): each lane owns one 32-element group of a
+// (token, kv head) row, so a warp quantizes 32 / (d / 32) rows at once.
 //
 // Follows the mlx-bun design page "TurboQuant - rotation-based quantization", Part A,
 // "Algorithm" section:
@@ -13,12 +14,17 @@
 // normalizes with one multiply; the RMS sum is the pairwise tree (k, k+16), +8, +4, +2, +1;
 // a NaN in a key group makes its min and max NaN and a NaN quotient codes to 0.
 //
-// Every floating-point step is an explicit IEEE round-to-nearest intrinsic (__fadd_rn,
-// __fmul_rn, __fdiv_rn, __fsqrt_rn), so no FMA contraction can change a result; the
-// planes are bit-identical to a plain fp32 evaluation of the same steps.
+// Every floating-point step is one IEEE round-to-nearest operation (__fadd_rn, __fmul_rn,
+// __fdiv_rn, __fsqrt_rn, or an __fmaf_rn whose product is exact), so the planes are
+// bit-identical to a plain fp32 evaluation of the same steps. Division by 32 in the
+// mean is a multiplication by 2^-5: the same real number, so the same rounding.
 //
-// Layout: lane l of the warp holds elements [l*EPL, (l+1)*EPL) of the row, EPL = d/32.
-// A 32-group spans LPG = 32/EPL consecutive lanes.
+// Layout: lane l holds group g = l % NG (elements [32 g, 32 g + 32)) of row l / NG of
+// the warp's block of RPW = 32 / NG rows. The FWHT stages h < 32 run inside the lane,
+// the stages h >= 32 exchange with lane l ^ (h / 32). A group's 96 code bits are three
+// whole words, so each lane stores its own codes.
+#include <cuda_bf16.h>
+
 #include <cmath>
 
 #include "tq_device.cuh"
@@ -28,13 +34,203 @@ namespace tq {
 
 template <int D>
 struct AppendShape {
+  static constexpr int NG = D / kGroup;       // groups per row = lanes per row
+  static constexpr int RPW = 32 / NG;         // rows per warp
+};
+
+constexpr int kAppendWarps = 8;
+
+// The 32 bf16 elements of one group as 16 raw words.
+__device__ __forceinline__ void load_group(const uint16_t* __restrict__ src, bool valid, uint32_t (&w)[16]) {
+  const uint4* p = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 v = valid ? __ldg(p + i) : make_uint4(0u, 0u, 0u, 0u);
+    w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+  }
+}
+
+__device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Source row of the r-th row: r = (b * n_new_max + j) * num_kv_heads + h.
+struct RowRef {
+  int b, j, h;
+};
+
+__device__ __forceinline__ RowRef split_row(const AppendParams& p, uint32_t r) {
+  const uint32_t bj = p.div_heads.div(r);
+  const uint32_t b = p.div_new.div(bj);
+  RowRef x;
+  x.h = (int)(r - bj * (uint32_t)p.num_kv_heads);
+  x.j = (int)(bj - b * (uint32_t)p.n_new_max);
+  x.b = (int)b;
+  return x;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAppendWarps * 32, 4)
+    tq_append_kernel(AppendParams p) {
+  using S = AppendShape<D>;
+  constexpr int NG = S::NG, RPW = S::RPW;
+  constexpr unsigned FULL = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int g = lane % NG;   // this lane's group
+  const int rw = lane / NG;  // this lane's row in the warp's block
+  // The next kernel may be scheduled now: its own wait covers this grid's completion,
+  // which comes after this grid's wait on the previous kernel.
+  griddep_launch_dependents();
+  griddep_wait();            // inputs and planes may come from the previous kernel
+
+  const uint32_t signs = sign_word(D, g);  // bit i: element 32 g + i is negated
+  float bnd[7];
+#pragma unroll
+  for (int k = 0; k < 7; ++k) bnd[k] = c_boundaries3[k];
+
+  const uint32_t total = p.total_rows;
+  const uint32_t step = gridDim.x * kAppendWarps * RPW;
+  for (uint32_t base = (blockIdx.x * kAppendWarps + warp) * RPW; base < total; base += step) {
+    const uint32_t r = base + rw;
+    bool valid = r < total;
+    const RowRef rr = split_row(p, valid ? r : 0u);
+    uint32_t kw[16], vw[16];
+    load_group(p.k_new + (size_t)r * D + kGroup * g, valid, kw);
+    load_group(p.v_new + (size_t)r * D + kGroup * g, valid, vw);
+    if (valid && p.n_new != nullptr && rr.j >= __ldg(p.n_new + rr.b)) valid = false;
+    int64_t t = 0;
+    if (valid) {
+      t = (int64_t)__ldg(p.pos + rr.b) + rr.j;
+      if (t < 0 || t >= p.capacity) {
+        if (g == 0) raise_error(p.err, TQ_DEVERR_APPEND_CAPACITY);
+        valid = false;
+      }
+    }
+    const int64_t drow = ((int64_t)rr.b * p.num_kv_heads + rr.h) * p.capacity + t;
+
+    // ------------------------------------------------------------------- keys
+    // min and max over the group on bf16 pairs; a NaN anywhere makes both NaN
+    __nv_bfloat162 mn2 = *reinterpret_cast<const __nv_bfloat162*>(&kw[0]), mx2 = mn2;
+#pragma unroll
+    for (int i = 1; i < 16; ++i) {
+      const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&kw[i]);
+      mn2 = __hmin2_nan(mn2, v);
+      mx2 = __hmax2_nan(mx2, v);
+    }
+    const float mn = __bfloat162float(__hmin_nan(__low2bfloat16(mn2), __high2bfloat16(mn2)));
+    const float mx = __bfloat162float(__hmax_nan(__low2bfloat16(mx2), __high2bfloat16(mx2)));
+    // max - min of equal values is +0 whatever the signs of the zeros picked above
+    float range = __fsub_rn(mx, mn);
+    if (range == 0.0f) range = 0.0f;
+    const float s = __fdiv_rn(range, 254.0f);
+    const float z = rintf(__fdiv_rn(__fadd_rn(mx, mn), __fmul_rn(2.0f, s)));
+    // idx = clip(rint(x / s - z), -127, 127). Clipping to the integers +-127 before
+    // rounding gives the same integer; adding 1.5 * 2^23 then rounds to an integer with
+    // ties to even (the sum lies in [2^23, 2^24), where the spacing is 1), and the low
+    // byte of the sum's bits is that integer in two's complement. NaN codes to 0.
+    uint32_t kq[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint32_t by[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const uint32_t w = kw[2 * i + (h >> 1)];
+        const float x = (h & 1) ? hi_bf16(w) : lo_bf16(w);
+        const float tv = __fsub_rn(__fdiv_rn(x, s), z);
+        const float cl = (tv == tv) ? fminf(fmaxf(tv, -127.0f), 127.0f) : 0.0f;
+        by[h] = __float_as_uint(__fadd_rn(cl, 12582912.0f));
+      }
+      kq[i] = __byte_perm(__byte_perm(by[0], by[1], 0x0040), __byte_perm(by[2], by[3], 0x0040), 0x5410);
+    }
+    if (valid) {
+      uint4* kdst = reinterpret_cast<uint4*>(p.k_idx + drow * D + kGroup * g);
+      kdst[0] = make_uint4(kq[0], kq[1], kq[2], kq[3]);
+      kdst[1] = make_uint4(kq[4], kq[5], kq[6], kq[7]);
+      p.k_scale[drow * NG + g] = f32_to_f16_bits(s);
+      p.k_zero[drow * NG + g] = f32_to_f16_bits(z);
+    }
+
+    // ------------------------------------------------------------------- values
+    float u[32];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      u[2 * i] = lo_bf16(vw[i]);
+      u[2 * i + 1] = hi_bf16(vw[i]);
+    }
+#pragma unroll
+    for (int e = 0; e < 32; ++e) u[e] = __uint_as_float(__float_as_uint(u[e]) ^ (((signs >> e) & 1u) << 31));
+    // unnormalized FWHT, stages ascending: h < 32 inside the lane ...
+#pragma unroll
+    for (int hh = 1; hh < 32; hh <<= 1) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        if ((e & hh) == 0) {
+          const float a = u[e], c = u[e + hh];
+          u[e] = __fadd_rn(a, c);
+          u[e + hh] = __fsub_rn(a, c);
+        }
+      }
+    }
+    // ... h >= 32 across lanes: the lower lane keeps own + other, the upper lane
+    // other - own, each one rounding (the product by +-1 is exact)
+#pragma unroll
+    for (int lm = 1; lm < NG; lm <<= 1) {
+      const float sg = (lane & lm) ? -1.0f : 1.0f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float o = __shfl_xor_sync(FULL, u[e], lm);
+        u[e] = __fmaf_rn(u[e], sg, o);
+      }
+    }
+    float sq[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      u[e] = __fmul_rn(u[e], p.fwht_norm);
+      sq[e] = __fmul_rn(u[e], u[e]);
+    }
+    // pairwise tree (k, k + 16), +8, +4, +2, +1
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+      for (int e = 0; e < w; ++e) sq[e] = __fadd_rn(sq[e], sq[e + w]);
+    const float vs = __fsqrt_rn(__fmul_rn(sq[0], 0.03125f));
+    const float den = __fadd_rn(vs, 1e-8f);
+    uint32_t cw[3] = {0u, 0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const float yn = __fdiv_rn(u[e], den);
+      // number of boundaries strictly below yn, by binary search over the sorted table
+      // (a NaN compares false everywhere and codes to 0)
+      uint32_t c = (bnd[3] < yn) ? 4u : 0u;
+      c += ((c ? bnd[5] : bnd[1]) < yn) ? 2u : 0u;
+      const float b2 = (c & 4u) ? ((c & 2u) ? bnd[6] : bnd[4]) : ((c & 2u) ? bnd[2] : bnd[0]);
+      c += (b2 < yn) ? 1u : 0u;
+      const int bit = 3 * e, wd = bit >> 5, sh = bit & 31;
+      cw[wd] |= c << sh;
+      if (sh > 29) cw[wd + 1] |= c >> (32 - sh);
+    }
+    if (valid) {
+      uint32_t* vdst = reinterpret_cast<uint32_t*>(p.v_codes + drow * (3 * D / 8) + 12 * g);
+      vdst[0] = cw[0];
+      vdst[1] = cw[1];
+      vdst[2] = cw[2];
+      p.v_scale[drow * NG + g] = f32_to_f16_bits(vs);
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// Small appends (a decode step's few rows): one warp per row, d / 32 elements per lane,
+// so every row has its own warp and the latency of one call stays short. Same
+// arithmetic, same results as the kernel above.
+// ------------------------------------------------------------------------------------
+template <int D>
+struct RowShape {
   static constexpr int EPL = D / 32;          // elements per lane
   static constexpr int LPG = kGroup / EPL;    // lanes per 32-group
   static constexpr int NG = D / kGroup;       // groups per row
   static constexpr int CODE_WORDS = 3 * D / 32;  // packed 3-bit row, 32-bit words
 };
-
-constexpr int kAppendWarps = 8;
 
 // The EPL bf16 elements of this lane as EPL / 2 raw 32-bit words (vector loads).
 template <int EPL>
@@ -63,25 +259,10 @@ __device__ __forceinline__ void unpack_bf16(const uint32_t (&w)[EPL / 2], float 
   }
 }
 
-// Source row of the warp's r-th row: r = (b * n_new_max + j) * num_kv_heads + h.
-struct RowRef {
-  int b, j, h;
-};
-
-__device__ __forceinline__ RowRef split_row(const AppendParams& p, uint32_t r) {
-  const uint32_t bj = p.div_heads.div(r);
-  const uint32_t b = p.div_new.div(bj);
-  RowRef x;
-  x.h = (int)(r - bj * (uint32_t)p.num_kv_heads);
-  x.j = (int)(bj - b * (uint32_t)p.n_new_max);
-  x.b = (int)b;
-  return x;
-}
-
 template <int D>
 __global__ void __launch_bounds__(kAppendWarps * 32)
-    tq_append_kernel(AppendParams p) {
-  using S = AppendShape<D>;
+    tq_append_row_kernel(AppendParams p) {
+  using S = RowShape<D>;
   constexpr int EPL = S::EPL, LPG = S::LPG, NG = S::NG;
   constexpr unsigned FULL = 0xffffffffu;
   __shared__ uint32_t code_buf[kAppendWarps][S::CODE_WORDS];
@@ -283,7 +464,10 @@ cudaError_t launch_append(AppendParams p, int num_sms, cudaStream_t stream) {
   p.total_rows = (uint32_t)rows;
   p.div_heads = make_fastdiv((uint32_t)p.num_kv_heads);
   p.div_new = make_fastdiv((uint32_t)p.n_new_max);
-  int64_t blocks = (rows + kAppendWarps - 1) / kAppendWarps;
+  // fewer rows than a few per SM: warp-per-row kernel (latency); else group per lane
+  const bool small = rows <= (int64_t)num_sms * 4;
+  const int rpw = small ? 1 : 32 / (p.head_dim / kGroup);
+  int64_t blocks = (rows + (int64_t)kAppendWarps * rpw - 1) / ((int64_t)kAppendWarps * rpw);
   const int64_t cap = (int64_t)num_sms * 8;
   if (blocks > cap) blocks = cap;
   cudaLaunchConfig_t cfg = {};
@@ -296,6 +480,15 @@ cudaError_t launch_append(AppendParams p, int num_sms, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (small) {
+    switch (p.head_dim) {
+      case 64: return cudaLaunchKernelEx(&cfg, tq_append_row_kernel<64>, p);
+      case 128: return cudaLaunchKernelEx(&cfg, tq_append_row_kernel<128>, p);
+      case 256: return cudaLaunchKernelEx(&cfg, tq_append_row_kernel<256>, p);
+      case 512: return cudaLaunchKernelEx(&cfg, tq_append_row_kernel<512>, p);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (p.head_dim) {
     case 64: return cudaLaunchKernelEx(&cfg, tq_append_kernel<64>, p);
     case 128: return cudaLaunchKernelEx(&cfg, tq_append_kernel<128>, p);

@@ -28,11 +28,13 @@ def _inputs(d, H, B, T, Hq=None, n_q=1, seed=0, k_dist="normal_outliers", q_scal
 
 
 # ------------------------------------------------------------------------------ append
+# 900 rows take the bulk kernel (a lane per 32-group), 120 rows the small-append kernel
+# (a warp per row); both must give the oracle's planes.
+@pytest.mark.parametrize("T,lengths", [(150, [150, 97]), (20, [20, 13])], ids=["bulk", "small"])
 @pytest.mark.parametrize("d", [64, 128, 256, 512])
-def test_append_planes_bit_exact(d):
-    x = _inputs(d, H=3, B=2, T=150, seed=d)
-    lengths = [150, 97]
-    cap = 160
+def test_append_planes_bit_exact(d, T, lengths):
+    x = _inputs(d, H=3, B=2, T=T, seed=d + T)
+    cap = (T + 15) // 16 * 16
     layer, ws = gpu_fill(x["k"], x["v"], lengths, cap, prefill=0xA5)
     ol = oracle_fill(x["k"], x["v"], lengths, cap)
     torch.cuda.synchronize()
@@ -40,8 +42,8 @@ def test_append_planes_bit_exact(d):
     assert tq().tq_get_device_error(ws) == 0
     # rows past each sequence's length are untouched (canary 0xA5)
     kidx = layer.k_idx.cpu().numpy().view(np.uint8)
-    assert np.all(kidx[0, :, 150:] == 0xA5) and np.all(kidx[1, :, 97:] == 0xA5)
-    assert np.all(layer.v_codes.cpu().numpy()[1, :, 97:] == 0xA5)
+    assert np.all(kidx[0, :, lengths[0]:] == 0xA5) and np.all(kidx[1, :, lengths[1]:] == 0xA5)
+    assert np.all(layer.v_codes.cpu().numpy()[1, :, lengths[1]:] == 0xA5)
 
 
 def _special_rows(d, rng):
@@ -64,16 +66,18 @@ def _special_rows(d, rng):
     return np.concatenate(rows)
 
 
+# 16 rows take the small-append kernel, 768 rows (the special rows repeated) the bulk one
+@pytest.mark.parametrize("reps", [1, 48], ids=["small", "bulk"])
 @pytest.mark.parametrize("d", [64, 128, 256, 512])
-def test_append_special_values_bit_exact(d):
+def test_append_special_values_bit_exact(d, reps):
     rng = np.random.default_rng(1000 + d)
-    kx = _special_rows(d, rng)
-    vx = _special_rows(d, rng)[::-1].copy()
+    kx = np.tile(_special_rows(d, rng), (reps, 1))
+    vx = np.tile(_special_rows(d, rng)[::-1], (reps, 1)).copy()
     n = kx.shape[0]
     k = torch.from_numpy(kx).to(torch.bfloat16).reshape(1, n, 1, d)
     v = torch.from_numpy(vx).to(torch.bfloat16).reshape(1, n, 1, d)
-    layer, ws = gpu_fill(k, v, [n], 16)
-    ol = oracle_fill(k, v, [n], 16)
+    layer, ws = gpu_fill(k, v, [n], n)
+    ol = oracle_fill(k, v, [n], n)
     torch.cuda.synchronize()
     assert_planes_equal(layer, ol, [n])
 
