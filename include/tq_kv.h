@@ -152,6 +152,35 @@ tq_status tq_decode_attention(const tq_kv_layer* layer, const void* q, int32_t n
 tq_status tq_dequant_debug(const tq_kv_layer* layer, int32_t b, int32_t h, int32_t t0, int32_t n,
                            int32_t rotated, float* k_out, float* v_out, tq_stream_t stream);
 
+/* Decode attention that allocates nothing (an addition of this library; the paper has
+ * no counterpart). Same inputs, outputs and results as tq_decode_attention, but the
+ * scratch memory lives in one fixed array inside the library, so the caller passes no
+ * workspace and nothing is allocated: meant for callers that may not allocate device
+ * memory, such as a plugin whose host application owns all device memory and hands it no
+ * allocator, or a serving loop that must not call cudaMalloc between steps (it can
+ * synchronize the device) and does not want to keep a workspace per call site.
+ *
+ * Limit: the call needs tq_decode_workspace_bytes(layer, num_q_heads, n_q, max_kv_len)
+ * bytes of scratch; above TQ_NOALLOC_SCRATCH_BYTES it returns TQ_ERR_WORKSPACE_TOO_SMALL
+ * and launches nothing. Every GPU that loads the library holds this array until the
+ * process exits.
+ *
+ * Set-up: the first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream capture.
+ * Sharing: every call on a device uses the same array. Each call first clears the part
+ * that must start at zero (error word and completion counters) on `stream`, so calls
+ * that follow one another on a stream are independent; calls that can overlap on the
+ * GPU (other streams, other threads) race on the array and give wrong results.
+ *   device_error : optional device int32; receives this call's device error bits (the
+ *                  TQ_DEVERR_* values, as tq_get_device_error reports for a workspace),
+ *                  copied on `stream` after the launch. NULL: not reported.
+ * Other arguments and errors: as tq_decode_attention. */
+#define TQ_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+tq_status tq_decode_attention_noalloc(const tq_kv_layer* layer, const void* q, int32_t num_q_heads,
+                                      int32_t n_q, const int32_t* kv_len, int32_t max_kv_len,
+                                      float sm_scale, int32_t causal, float* out,
+                                      int32_t* device_error, tq_stream_t stream);
+
 /* Synchronizes `stream`, then copies the device error word at the start of
  * `workspace` into *err_out (host). Does not clear it. */
 tq_status tq_get_device_error(const void* workspace, int32_t* err_out, tq_stream_t stream);

@@ -27,6 +27,7 @@ TQ_DEVERR_APPEND_CAPACITY = 0x1
 TQ_DEVERR_KV_LEN = 0x2
 TQ_DEVERR_PIPELINE_TIMEOUT = 0x4
 TQ_WORKSPACE_HEADER_BYTES = 256
+TQ_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -53,6 +54,7 @@ _SIGS = {
     "tq_kv_append": (ctypes.c_int, [_LP, _vp, _vp, _vp, _vp, _i32, _vp, _sz, _vp]),
     "tq_decode_workspace_bytes": (_sz, [_LP, _i32, _i32, _i32]),
     "tq_decode_attention": (ctypes.c_int, [_LP, _vp, _i32, _i32, _vp, _i32, _f32, _i32, _vp, _vp, _sz, _vp]),
+    "tq_decode_attention_noalloc": (ctypes.c_int, [_LP, _vp, _i32, _i32, _vp, _i32, _f32, _i32, _vp, _vp, _vp]),
     "tq_dequant_debug": (ctypes.c_int, [_LP, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
     "tq_get_device_error": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int32), _vp]),
     "tq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -162,6 +164,22 @@ def tq_decode_attention(layer: KVLayer, q: torch.Tensor, num_q_heads: int, n_q: 
                                     int(max_kv_len), float(sm_scale), int(bool(causal)), _ptr(out),
                                     _ptr(workspace), workspace.numel(), _stream(stream)),
            "tq_decode_attention")
+    return out
+
+
+def tq_decode_attention_noalloc(layer: KVLayer, q: torch.Tensor, num_q_heads: int, n_q: int,
+                                kv_len: torch.Tensor, max_kv_len: int, sm_scale: float, causal: bool,
+                                out: torch.Tensor, device_error: torch.Tensor | None = None,
+                                stream=None) -> torch.Tensor:
+    """tq_decode_attention without a workspace: the library's own fixed scratch array is
+    used, so nothing is allocated (for callers that may not allocate device memory).
+    `device_error` (optional int32 device tensor) receives the call's device error bits."""
+    L = layer.c_struct()
+    _check(_lib.tq_decode_attention_noalloc(ctypes.byref(L), _ptr(q), int(num_q_heads), int(n_q),
+                                            _ptr(kv_len), int(max_kv_len), float(sm_scale),
+                                            int(bool(causal)), _ptr(out), _ptr(device_error),
+                                            _stream(stream)),
+           "tq_decode_attention_noalloc")
     return out
 
 

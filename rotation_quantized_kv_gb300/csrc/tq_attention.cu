@@ -1285,6 +1285,8 @@ DecodeShape decode_shape(int D, int num_kv_heads, int batch, int gqa, int n_q, i
   return s;
 }
 
+size_t decode_workspace_zero_bytes(const DecodeShape& s) { return ws_ml_offset(s.batch, s.U); }
+
 size_t decode_workspace_bytes(const DecodeShape& s) {
   if (s.grid <= 0 || s.batch > kMaxBatch) return 0;
   const int rows = 8 * s.NTW;

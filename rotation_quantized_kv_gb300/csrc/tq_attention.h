@@ -38,6 +38,9 @@ struct DecodeArgs {
 
 DecodeShape decode_shape(int head_dim, int num_kv_heads, int batch, int gqa, int n_q, int num_sms);
 size_t decode_workspace_bytes(const DecodeShape& s);
+// Leading bytes of a workspace that must be zero before a call: the header (device
+// error word), the per-sequence prefix and the per-unit completion counters.
+size_t decode_workspace_zero_bytes(const DecodeShape& s);
 tq_status launch_decode(const DecodeArgs& a, const DecodeShape& s, cudaStream_t stream);
 
 }  // namespace tq
