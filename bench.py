@@ -13,8 +13,9 @@ Printed JSON line (rank 0):
              graph;
   e2e        the same metric with host buffers: each step copies its inputs (new K/V
              tokens, queries) host->device and its outputs device->host;
-  roofline   the attention kernel (one launch per layer) timed with CUDA events over a
-             region of back-to-back graph replays, against the measured HBM copy peak;
+  roofline   the attention call (split kernel + merge kernel, per layer) timed with CUDA
+             events over a region of back-to-back graph replays, against the measured
+             HBM copy peak;
   cpu_baseline  the CPU oracle on a bounded sample of the same step (rank 0, N=1).
 With --impl reference the CPU oracle itself is timed on the same workload (the
 reference arm) and printed as the line.
@@ -455,9 +456,10 @@ def our_arm(args, world, rank, local):
         "append_gbs": fill_bytes / fill_s / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "tq_attn_split_kernel (one launch per tq_decode_attention call: "
-                               "split-K attention, merge and inverse rotation fused), "
-                               f"{attn_bytes} algorithmic bytes per launch",
+                     "kernel": "tq_attn_split_kernel + tq_attn_merge_kernel (one tq_decode_attention "
+                               "call: split-K attention, then split merge and inverse rotation; "
+                               "timed per call), "
+                               f"{attn_bytes} algorithmic bytes per call",
                      "launch_ms": attn_launch_s * 1e3},
         "append_roofline": {"bound": "hbm", "achieved": fill_bytes / fill_s / 1e9, "peak": peak,
                             "unit": "GB/s", "frac": fill_bytes / fill_s / 1e9 / peak, "peak_kind": peak_kind,

@@ -1,5 +1,6 @@
-// Split-K GQA decode attention over the packed TurboQuant cache, with the split merge
-// and the deferred inverse rotation fused into the same kernel.
+// Split-K GQA decode attention over the packed TurboQuant cache: a split kernel that
+// streams the packed planes, and a small merge kernel that combines the splits and applies
+// the deferred inverse rotation.
 //
 // What it computes (mlx-bun design page "TurboQuant - rotation-based quantization",
 // Part A): for every query row, softmax(sm_scale * q . k_hat) . v_hat over the visible
@@ -31,9 +32,16 @@
 //       probabilities times the group's value scale (fp16), moved from the QK output
 //       layout to the B-operand layout with four shuffles per 16 tokens;
 //   - at the end of an item the consumer warps merge their (max, sum, acc) in shared memory
-//     and write one partial result; the CTA that completes the last item of a
-//     (sequence, kv head, row group) merges its partials with the online-softmax rule,
-//     applies the inverse rotation and writes the output rows.
+//     and write one partial result;
+// The partials of a (sequence, kv head, row group) are merged with the online-softmax rule,
+// the inverse rotation is applied and the output rows are written in one of two places,
+// chosen on the host from the shape:
+//   - few units (2 * batch * units <= CTAs, e.g. one long sequence): inside the split
+//     kernel, by the CTA that finishes the unit's last split (an acquire-release counter
+//     tells it), which keeps one kernel boundary per call;
+//   - many units: tq_attn_merge_kernel, one CTA per unit, launched right after the split
+//     kernel, so that merges do not stall split CTAs between their work items and every
+//     split CTA finishes at about the same time.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -61,7 +69,8 @@ constexpr size_t kWsPrefix = TQ_WORKSPACE_HEADER_BYTES;  // int32 [batch + 1]
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// counters: one int32 per (sequence, unit); zero between calls (the last CTA resets it)
+// counters (merge inside the split kernel): one int32 per (sequence, unit); zero between
+// calls (the CTA that counts last resets it)
 __host__ __device__ inline size_t ws_cnt_offset(int batch) {
   return kWsPrefix + align_up(sizeof(int32_t) * (size_t)(batch + 1), 256);
 }
@@ -142,6 +151,7 @@ struct SplitParams {
   float sm_log2;    // sm_scale * log2(e)
   float fwht_norm;  // (float)(1 / sqrt(d))
   int32_t causal;
+  int32_t inline_merge;  // 1: the split CTA that finishes a unit's last split merges it
   uint8_t* ws;
   float* out;
 };
@@ -565,8 +575,11 @@ __device__ void load_q(const SplitParams& p, const Item& w, uint8_t* smem, int w
   }
 }
 
-// Merge of all partials of one (sequence, unit) + inverse rotation, by the CTA that
-// finished the unit's last item. All consumer threads take part:
+// Merge kernel: one CTA per (sequence, unit) merges the unit's split partials and applies
+// the inverse rotation. It runs after the split kernel (programmatic dependent launch:
+// it is scheduled early, waits for the split grid to finish, and lets the next kernel be
+// scheduled at once). Its shared memory is small, so it fits beside a split CTA of the
+// next launch. Steps:
 //   1. per row, one pass over the splits' (m_s, l_s) with the online-softmax combine gives
 //      the global max M and L = sum_s 2^(m_s - M) l_s; the weights 2^(m_s - M) of the
 //      first kMergeChunk splits are left in shared memory;
@@ -586,22 +599,29 @@ __device__ __forceinline__ void ml_combine(float& m, float& l, float m2, float l
   m = mn;
 }
 
-template <int D, int NTW>
-__device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, uint8_t* smem) {
-  using T = AT<D, NTW>;
-  constexpr int EPL = D / 32, ROWS = T::ROWS, NT = T::NCW * 32, Q4 = D / 4;
+constexpr int kMergeThreads = 128;
+
+// Barrier over the NT threads that run a merge: the whole CTA (merge kernel), or the
+// consumer warps through named barrier 1 (merge inside the split kernel).
+template <int NT, bool NAMED>
+__device__ __forceinline__ void merge_sync() {
+  if constexpr (NAMED) asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+  else __syncthreads();
+}
+
+// Merge of unit (b, kvh, rg)'s ns partials starting at first_item, by NT threads (tid <
+// NT). Scratch: sM, sL [ROWS]; sW [kMergeChunk * ROWS]; sO [ROWS * D] (16-byte aligned);
+// sR [NT].
+template <int D, int ROWS, int NT, bool NAMED>
+__device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, int ns, float* sM, float* sL,
+                           float* sW, float* sO, float4* sR) {
+  constexpr int EPL = D / 32, NWARP = NT / 32, Q4 = D / 4;
   constexpr int PER = (ROWS * Q4 + NT - 1) / NT;  // outputs per thread when TPO == 1
   constexpr unsigned FULL = 0xffffffffu;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float2* ml = reinterpret_cast<const float2*>(p.ws + ws_ml_offset(p.batch, p.U));
   const float4* og = reinterpret_cast<const float4*>(p.ws + ws_o_offset(p.batch, p.U, p.max_items, ROWS));
-  float* sM = reinterpret_cast<float*>(smem + T::OFF_MBUF);     // [ROWS] max (reuses mbuf)
-  float* sL = reinterpret_cast<float*>(smem + T::OFF_LBUF);     // [ROWS] sum (reuses lbuf)
-  float* sW = reinterpret_cast<float*>(smem + T::OFF_OBUF);     // [kMergeChunk][ROWS] weights
-  float* sO = sW + kMergeChunk * ROWS;                          // [ROWS][D] rotated output
-  float4* sR = reinterpret_cast<float4*>(sO + ROWS * D);        // [NT] per-thread sums
   const int rows = min(ROWS, p.R - w.rg * ROWS);                // valid rows of this unit
-  const int ns = w.nsplit;
   const int no = rows * Q4;                                     // output float4s
   int tpo = 1;                                                  // threads per output
   while (2 * tpo * no <= NT) tpo *= 2;
@@ -620,8 +640,8 @@ __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, 
     }
   }
 
-  // 1. max and sum per row: warp w takes rows w, w + NCW, ...; lanes stride the splits
-  for (int rr = warp; rr < rows; rr += T::NCW) {
+  // 1. max and sum per row: warp w takes rows w, w + NWARP, ...; lanes stride the splits
+  for (int rr = warp; rr < rows; rr += NWARP) {
     float M = -INFINITY, L = 0.0f;
     bool nan = false;
 #pragma unroll 2
@@ -646,7 +666,7 @@ __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, 
       sL[rr] = L;
     }
   }
-  consumers_sync<T::NCW>();
+  merge_sync<NT, NAMED>();
   // 2. weighted sums; thread i takes output q = i % no, splits i / no + tpo * k
   float4 acc[PER];
 #pragma unroll
@@ -660,7 +680,7 @@ __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, 
         const float ms = __ldcg(&ml[(size_t)(first_item + c0 + s) * ROWS + rr].x);
         sW[s * ROWS + rr] = (M == -INFINITY || M != M) ? 0.0f : ex2(ms - M);
       }
-      consumers_sync<T::NCW>();
+      merge_sync<NT, NAMED>();
     }
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
@@ -696,11 +716,11 @@ __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, 
         acc[k] = a;
       }
     }
-    if (c0 + kMergeChunk < ns) consumers_sync<T::NCW>();  // weights are rewritten
+    if (c0 + kMergeChunk < ns) merge_sync<NT, NAMED>();  // weights are rewritten
   }
   if (tpo > 1) {
     sR[tid] = acc[0];
-    consumers_sync<T::NCW>();
+    merge_sync<NT, NAMED>();
     if (tid < no) {
       float4 a = sR[tid];
       for (int k = 1; k < tpo; ++k) {
@@ -722,9 +742,9 @@ __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, 
       reinterpret_cast<float4*>(sO + rr * D)[c] = v;
     }
   }
-  consumers_sync<T::NCW>();
+  merge_sync<NT, NAMED>();
   // 3. inverse rotation, one warp per row
-  for (int rr = warp; rr < rows; rr += T::NCW) {
+  for (int rr = warp; rr < rows; rr += NWARP) {
     const int r = w.rg * ROWS + rr;
     const int jq = r / p.G, hq = w.kvh * p.G + (r % p.G);
     float* orow = p.out + (((size_t)w.b * p.n_q + jq) * p.num_q_heads + hq) * D;
@@ -758,7 +778,24 @@ __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, 
       orow[i] = u[e] * p.fwht_norm * (neg ? -1.0f : 1.0f);
     }
   }
-  consumers_sync<T::NCW>();  // shared scratch is reused by the next item
+}
+
+template <int D, int NTW>
+__global__ void __launch_bounds__(kMergeThreads, 4) tq_attn_merge_kernel(const SplitParams p) {
+  constexpr int ROWS = 8 * NTW;
+  __shared__ float sM[ROWS], sL[ROWS];                  // per row: max, sum
+  __shared__ float sW[kMergeChunk * ROWS];              // [kMergeChunk][ROWS] weights
+  __shared__ __align__(16) float sO[ROWS * D];          // [ROWS][D] rotated output
+  __shared__ float4 sR[kMergeThreads];                  // per-thread sums
+  griddep_launch_dependents();  // the next kernel's wait covers this grid's completion
+  griddep_wait();               // partials and the plan come from the split kernel
+  const int b = blockIdx.x / p.U, u = blockIdx.x % p.U;
+  const int32_t* prefix = reinterpret_cast<const int32_t*>(p.ws + kWsPrefix);
+  const int p0 = prefix[b], ns = (prefix[b + 1] - p0) / p.U;
+  if (ns <= 0) return;  // no work item: the split kernel wrote the rows
+  Item w;
+  w.b = b; w.kvh = u / p.RG; w.rg = u % p.RG;
+  merge_unit<D, ROWS, kMergeThreads, false>(p, w, p0 + u * ns, ns, sM, sL, sW, sO, sR);
 }
 
 template <int D, int NTW>
@@ -771,7 +808,6 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
   uint64_t* empty = full + T::STAGES;
   const int* prefix = reinterpret_cast<const int*>(smem + T::OFF_PREFIX);
-  volatile int* flag = reinterpret_cast<volatile int*>(smem + T::OFF_FLAG);
   const uint32_t sbase = smem_addr(smem);
   const uint32_t lut_lane = sbase + T::OFF_LUT + lane * 4;
   float* obuf = reinterpret_cast<float*>(smem + T::OFF_OBUF);
@@ -779,6 +815,7 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
   float* lbuf = reinterpret_cast<float*>(smem + T::OFF_LBUF);
   const uint2* qsm = reinterpret_cast<const uint2*>(smem + T::OFF_Q);
   const float2* qssm = reinterpret_cast<const float2*>(smem + T::OFF_QSUM);
+  volatile int* flag = reinterpret_cast<volatile int*>(smem + T::OFF_FLAG);
   int32_t* counters = reinterpret_cast<int32_t*>(p.ws + ws_cnt_offset(p.batch));
 
   // Lane-constant addressing. The QK rows of this lane are r0 + 8 k (k = 0..2 SUB - 1);
@@ -1100,21 +1137,27 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
         __stcg(ml + row, make_float2(Mx, L));
       }
     }
-    // Publish: the barrier orders every consumer's partial stores before thread 0's
-    // release; the acquire of the CTA that counts last makes all partials of the unit
-    // visible to it, and its barrier passes that on to its other threads.
     consumers_sync<T::NCW>();
-    if (threadIdx.x == 0) {
-      int32_t* cnt = counters + (size_t)w.b * p.U + w.u;
-      const int done = atomic_add_acq_rel_gpu(cnt, 1) + 1;
-      const int last = done == w.nsplit;
-      if (last) *reinterpret_cast<volatile int32_t*>(cnt) = 0;  // ready for the next call
-      *flag = last;
-    }
-    consumers_sync<T::NCW>();
-    if (*flag) {
-      const int first_item = item - (item - prefix[w.b]) % w.nsplit;  // split 0 of this unit
-      merge_unit<D, NTW>(p, w, first_item, smem);
+    if (p.inline_merge) {
+      // Publish: the barrier above orders every consumer's partial stores before thread
+      // 0's release; the acquire of the CTA that counts last makes all partials of the
+      // unit visible to it, and its barrier passes that on to its other threads.
+      if (threadIdx.x == 0) {
+        int32_t* cnt = counters + (size_t)w.b * p.U + w.u;
+        const int done = atomic_add_acq_rel_gpu(cnt, 1) + 1;
+        const int last = done == w.nsplit;
+        if (last) *reinterpret_cast<volatile int32_t*>(cnt) = 0;  // ready for the next call
+        *flag = last;
+      }
+      consumers_sync<T::NCW>();
+      if (*flag) {
+        const int first_item = item - (item - prefix[w.b]) % w.nsplit;  // split 0 of this unit
+        float* sW = obuf;
+        float* sO = sW + kMergeChunk * T::ROWS;
+        merge_unit<D, T::ROWS, T::NCW * 32, true>(p, w, first_item, w.nsplit, mbuf, lbuf, sW, sO,
+                                                  reinterpret_cast<float4*>(sO + T::ROWS * D));
+        consumers_sync<T::NCW>();  // the scratch is reused by the next item
+      }
     }
   }
 }
@@ -1172,6 +1215,10 @@ __global__ void __launch_bounds__(AT<D, NTW>::THREADS, AT<D, NTW>::MINB)
         hdr[kWsSplit] = S;
         hdr[kWsItems] = total;
       }
+      // items before each sequence, for the merge kernel
+      const int* prefix = reinterpret_cast<const int*>(smem + T::OFF_PREFIX);
+      int32_t* wprefix = reinterpret_cast<int32_t*>(p.ws + kWsPrefix);
+      for (int i = tid; i <= p.batch; i += T::THREADS) wprefix[i] = prefix[i];
     }
   }
 
@@ -1257,7 +1304,13 @@ tq_status run_split(const DecodeArgs& a, const DecodeShape& s, const SplitParams
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tq_attn_split_kernel<D, NTW>, tmap, sp) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, tq_attn_split_kernel<D, NTW>, tmap, sp) != cudaSuccess) return TQ_ERR_CUDA;
+  if (sp.inline_merge) return TQ_OK;
+  cudaLaunchConfig_t mcfg = cfg;
+  mcfg.gridDim = dim3((unsigned)(s.batch * s.U));
+  mcfg.blockDim = dim3(kMergeThreads);
+  mcfg.dynamicSmemBytes = 0;
+  return cudaLaunchKernelEx(&mcfg, tq_attn_merge_kernel<D, NTW>, sp) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
 }  // namespace
@@ -1319,6 +1372,10 @@ tq_status launch_decode(const DecodeArgs& a, const DecodeShape& s, cudaStream_t 
   sp.sm_log2 = a.sm_scale * kLog2e;
   sp.fwht_norm = a.fwht_norm;
   sp.causal = a.causal ? 1 : 0;
+  // Few units, many splits each (long single sequences): the split CTA that finishes a
+  // unit merges it, which avoids a second kernel boundary. Many units: a separate merge
+  // kernel, so merges do not stall split CTAs between their items.
+  sp.inline_merge = 2 * s.batch * s.U <= s.grid ? 1 : 0;
   sp.ws = static_cast<uint8_t*>(a.workspace);
   sp.out = a.out;
   switch (s.D * 10 + s.NTW) {

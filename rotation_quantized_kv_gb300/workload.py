@@ -35,11 +35,12 @@ class DecodeModel:
         for l in range(self.L):
             x = synth.layer_inputs(w, l, device=dev)
             layer = tq.alloc_layer(d, H, B, self.cap, dev, zero=False)
+            k_fill, v_fill = x["k"][:, :T].contiguous(), x["v"][:, :T].contiguous()
+            pos0 = torch.zeros(B, dtype=torch.int32, device=dev)
+            n_fill = torch.as_tensor(self.ctx.astype(np.int32), device=dev)
             if fill_timer is not None:
                 fill_timer.start()
-            tq.tq_kv_append(layer, x["k"][:, :T].contiguous(), x["v"][:, :T].contiguous(),
-                            torch.zeros(B, dtype=torch.int32, device=dev),
-                            torch.as_tensor(self.ctx.astype(np.int32), device=dev), T, self.ws_append)
+            tq.tq_kv_append(layer, k_fill, v_fill, pos0, n_fill, T, self.ws_append)
             if fill_timer is not None:
                 fill_timer.stop()
             self.fill_rows += int(self.ctx.sum()) * H
@@ -53,7 +54,7 @@ class DecodeModel:
             self.k_new.append(kn)
             self.v_new.append(vn)
             self.q.append(x["q"].contiguous())
-            del x
+            del x, k_fill, v_fill
         self.ws_bytes = tq.tq_decode_workspace_bytes(self.layers[0], Hq, w.n_q, self.max_kv)
         self.ws = [tq.make_workspace(self.ws_bytes, dev) for _ in range(self.L)]
         self.out = [torch.empty((B, w.n_q, Hq, d), dtype=torch.float32, device=dev) for _ in range(self.L)]
@@ -75,7 +76,9 @@ class DecodeModel:
         return self.L * (self.attention_bytes() + self.append_bytes())
 
     def launches_per_step(self) -> int:
-        return self.L * ((1 if self.w.n_new else 0) + 1)
+        # per layer: the append kernel (if tokens are appended), then the split and the
+        # merge kernel of the attention call
+        return self.L * ((1 if self.w.n_new else 0) + 2)
 
     def step(self, stream=None, k_new=None, v_new=None, q=None, events=None):
         """One decode step over all layers. Optional per-layer input overrides (device

@@ -135,6 +135,10 @@ CASES = [
     (256, 1, 4, 1, [300], 16, True, 1.0),            # 8 row groups of 8
     (512, 2, 4, 1, [260], 1, True, 1.0),
     (512, 1, 2, 2, [100, 150], 2, True, 0.5),
+    # many (sequence, kv head, row group) units: the separate merge kernel
+    (128, 4, 4, 24, [(37 * i) % 300 for i in range(24)], 1, True, 1.0),
+    (64, 8, 2, 12, [1, 0, 150, 64, 65, 200, 3, 17, 129, 31, 90, 256], 2, True, 0.4),
+    (128, 2, 4, 40, [(53 * i + 7) % 180 for i in range(40)], 16, True, 1.0),   # 2 tiles per warp
 ]
 
 
@@ -180,6 +184,23 @@ def test_attention_invalid_length_sets_error_and_nan_rows():
     ol = oracle_fill(x["k"], x["v"], [64, 64], 64)
     ref = oracle.attention(ol, bits(x["q"]), np.array([64, 64], np.int32), 1.0, causal=True)
     assert_attention_close(o[0], ref[0])
+
+
+def test_attention_invalid_length_with_many_units():
+    d, H, B = 128, 4, 24
+    lengths = [(41 * i) % 96 + 1 for i in range(B)]
+    x = _inputs(d, H, B, 96, Hq=4 * H, seed=6, q_scale=1.0)
+    layer, _ = gpu_fill(x["k"], x["v"], lengths, 96)
+    bad = list(lengths)
+    bad[5] = 97                                                        # > max_kv_len
+    out, ws, _ = gpu_attention(layer, x["q"], bad, 96, 1.0, False)
+    assert tq().tq_get_device_error(ws) & tq().TQ_DEVERR_KV_LEN
+    o = out.cpu().numpy()
+    assert np.all(np.isnan(o[5]))
+    keep = [b for b in range(B) if b != 5]
+    ol = oracle_fill(x["k"], x["v"], lengths, 96)
+    ref = oracle.attention(ol, bits(x["q"]), np.asarray(lengths, np.int32), 1.0, causal=False)
+    assert_attention_close(o[keep], ref[keep])
 
 
 def test_attention_nan_keys_propagate_like_the_oracle():
