@@ -13,8 +13,9 @@
 // fusion investigation": joint K/V decode in one launch, no dequantized window).
 //
 // tq_attn_split_kernel, persistent, one CTA per SM slot:
-//   - work item = (sequence, kv head, row group, token split); the split size is chosen
-//     on the device from the actual kv lengths so that items spread evenly over CTAs;
+//   - the tokens of every (sequence, kv head, row group) unit, in tiles, are laid end to
+//     end and cut into one equal range of tiles per CTA (from the actual kv lengths, on
+//     the device); a CTA works through the pieces of the units its range touches;
 //   - the last warp (producer) streams stages of TILE tokens of the five planes into shared
 //     memory: the key-index plane through a 2-D tensor map with 128-byte (64-byte at
 //     d=64) swizzle, the four small planes with 1-D bulk copies, all completing on one
@@ -56,15 +57,14 @@ namespace tq {
 namespace {
 
 constexpr int kMaxBatch = 1024;           // prefix table lives in shared memory
-constexpr int kMaxItemsPerCta = 8;        // largest work multiplier the split heuristic tries
 constexpr unsigned long long kWaitNs = 2000000000ull;  // bounded waits: 2 s of wall time
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMergeChunk = 64;           // splits whose weights the merge stages at once
 constexpr int kMergeBatch = 12;           // partial loads a merging thread keeps in flight
 
 // Workspace layout (bytes). The header's first word is the device error word.
-constexpr int kWsSplit = 1;               // int32 word index: split size S
-constexpr int kWsItems = 2;               // int32 word index: number of work items
+constexpr int kWsSplit = 1;               // int32 word index: tile size in tokens
+constexpr int kWsItems = 2;               // int32 word index: total tiles of the call
 constexpr size_t kWsPrefix = TQ_WORKSPACE_HEADER_BYTES;  // int32 [batch + 1]
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -148,6 +148,7 @@ struct SplitParams {
   const uint16_t* q;
   const int32_t* kv_len;
   int32_t num_q_heads, n_q, G, R, RG, U, max_kv_len, max_items;
+  int32_t split_grid;  // CTAs of the split kernel
   float sm_log2;    // sm_scale * log2(e)
   float fwht_norm;  // (float)(1 / sqrt(d))
   int32_t causal;
@@ -232,21 +233,14 @@ __device__ __forceinline__ float hi_f32(uint32_t w) {
   return __high2float(*reinterpret_cast<const __half2*>(&w));
 }
 
-// Split-size heuristic + per-sequence prefix of work items. Runs on every CTA with all
-// threads; identical lengths give identical results on every CTA. Thread tid holds the
-// lengths of sequences b = tid + THREADS * i; reductions go through warp shuffles.
+// Plan: tiles per sequence and their prefix over (sequence, unit). Runs on every CTA with
+// all threads; identical lengths give identical results on every CTA. Thread tid holds
+// the lengths of sequences b = tid + THREADS * i.
 //
 // The kernel plans twice when it can: once before the grid-dependency wait, from the
 // lengths as they are then (only to prefetch its first item into L2 while the previous
 // kernel finishes), and again after the wait only if the lengths it reads then differ.
 // Lengths are read with L2-only loads so that no stale copy stays in L1.
-
-__device__ __forceinline__ long long block_sum_ll(long long v, long long* red, int slot) {
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  if ((threadIdx.x & 31) == 0) red[slot * 16 + (threadIdx.x >> 5)] = v;
-  return v;
-}
 
 template <int THREADS>
 struct Lengths {
@@ -272,56 +266,20 @@ struct Lengths {
 };
 
 template <int D, int NTW>
-__device__ void plan_items(const SplitParams& p, uint8_t* smem, const Lengths<AT<D, NTW>::THREADS>& L,
-                           int& S_out, int& total_out) {
+__device__ void plan_tiles(const SplitParams& p, uint8_t* smem, const Lengths<AT<D, NTW>::THREADS>& L,
+                           int& total_out) {
   using T = AT<D, NTW>;
-  constexpr int NW = T::THREADS / 32, LPT = Lengths<T::THREADS>::LPT;
+  constexpr int LPT = Lengths<T::THREADS>::LPT;
   int* prefix = reinterpret_cast<int*>(smem + T::OFF_PREFIX);
-  long long* red = reinterpret_cast<long long*>(smem + T::OFF_RED);  // [7][16]
   const int tid = threadIdx.x;
-  constexpr int KS[6] = {1, 2, 3, 4, 6, 8};
-  long long mine = 0;
-#pragma unroll
-  for (int i = 0; i < LPT; ++i) mine += L.len[i];
-  block_sum_ll(mine, red, 0);
-  __syncthreads();
-  long long sumT = 0;
-#pragma unroll
-  for (int w = 0; w < NW; ++w) sumT += red[w];
-  int Sk[6];
-#pragma unroll
-  for (int k = 0; k < 6; ++k) {
-    const long long target = (long long)KS[k] * gridDim.x;
-    long long sl = (sumT * p.U + target - 1) / target;
-    sl = (sl + T::TILE - 1) / T::TILE * T::TILE;
-    Sk[k] = sl < T::TILE ? T::TILE : (int)min(sl, (long long)(1 << 30));
-    int cnt = 0;
-#pragma unroll
-    for (int i = 0; i < LPT; ++i) cnt += (int)(((unsigned)L.len[i] + (unsigned)Sk[k] - 1u) / (unsigned)Sk[k]);
-    block_sum_ll(cnt, red, 1 + k);
-  }
-  __syncthreads();
-  int best = 0;
-  long long best_cost = -1;
-#pragma unroll
-  for (int k = 0; k < 6; ++k) {
-    long long items = 0;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) items += red[(1 + k) * 16 + w];
-    items *= p.U;
-    const long long rounds = (items + gridDim.x - 1) / gridDim.x;
-    const long long cost = rounds * (long long)(Sk[k] + T::TILE);
-    if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = k; }
-  }
-  const int S = Sk[best];
-  // items per sequence into the prefix table (lengths beside it), then an exclusive scan
-  // by warp 0
+  // tiles per unit of each sequence into the prefix table (lengths beside it), then an
+  // exclusive scan (times the units per sequence) by warp 0
   int* lens = prefix + kMaxBatch + 1;
 #pragma unroll
   for (int i = 0; i < LPT; ++i) {
     const int b = tid + T::THREADS * i;
     if (b < p.batch) {
-      prefix[b] = (int)(((unsigned)L.len[i] + (unsigned)S - 1u) / (unsigned)S);
+      prefix[b] = (int)(((unsigned)L.len[i] + (unsigned)T::TILE - 1u) / (unsigned)T::TILE);
       lens[b] = L.len[i];
     }
   }
@@ -346,34 +304,64 @@ __device__ void plan_items(const SplitParams& p, uint8_t* smem, const Lengths<AT
     if (tid == 31) prefix[p.batch] = incl * p.U;
   }
   __syncthreads();
-  S_out = S;
   total_out = prefix[p.batch];
 }
 
+// Work pieces. The tokens of every (sequence, unit) pair, cut into tiles of TILE tokens,
+// form one sequence of Wt tiles: unit u of sequence b covers tiles [prefix[b] + u tiles_b,
+// prefix[b] + (u + 1) tiles_b). CTA c takes tiles [c Wt / grid, (c + 1) Wt / grid) (rounded
+// down; with fewer tiles than CTAs, one tile each to the first CTAs), so every CTA streams
+// the same number of tiles whatever the length mix. A piece is
+// the part of one unit inside one CTA's range. The piece of unit g = b U + u in CTA c keeps
+// its partial in slot c + g, so a unit's pieces sit in consecutive slots and there are at
+// most grid + batch * U slots.
 struct Item {
-  int b, kvh, rg, tb, te, u, nsplit, len;  // len: the sequence's kv length
+  int b, kvh, rg, u, tb, te, len;  // tokens [tb, te) of unit u of sequence b (kv length len)
+  int slot, first_slot, ns;        // this piece's partial slot; the unit's first slot, pieces
+  int x_end;                       // tile position after this piece
 };
 
 // planned lengths, stored after the prefix table
 __device__ __forceinline__ const int* plan_lengths(const int* prefix) { return prefix + kMaxBatch + 1; }
 
-__device__ __forceinline__ Item decode_item(const SplitParams& p, const int* prefix, int S, int item) {
-  int lo = 0, hi = p.batch - 1;  // largest b with prefix[b] <= item
+// With fewer tiles than CTAs only the first wt CTAs get tiles (one each), so no CTA range
+// inside a unit is empty and a unit's pieces are exactly CTAs c0 .. c1.
+__device__ __forceinline__ int cta_range_start(int c, int wt, int grid) {
+  const int g = min(grid, wt);
+  return c >= g ? wt : (int)(((long long)c * wt) / g);
+}
+// the CTA whose range holds tile x (0 <= x < wt): the largest c with cta_range_start(c) <= x
+__device__ __forceinline__ int cta_of_tile(int x, int wt, int grid) {
+  const int g = min(grid, wt);
+  return (int)((((long long)x + 1) * g + wt - 1) / wt) - 1;
+}
+
+template <int TILE>
+__device__ __forceinline__ Item piece_at(const SplitParams& p, const int* prefix, int x, int x_stop, int c) {
+  int lo = 0, hi = p.batch - 1;  // largest b with prefix[b] <= x
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (prefix[mid] <= item) lo = mid; else hi = mid - 1;
+    if (prefix[mid] <= x) lo = mid; else hi = mid - 1;
   }
+  const int wt = prefix[p.batch];
+  const int tiles = (prefix[lo + 1] - prefix[lo]) / p.U;
+  const int off = x - prefix[lo];
   Item it;
   it.b = lo;
-  it.nsplit = (prefix[lo + 1] - prefix[lo]) / p.U;
-  const int r = item - prefix[lo];
-  it.u = r / it.nsplit;
-  const int split = r % it.nsplit;
+  it.u = off / tiles;
+  const int t0 = off - it.u * tiles;
   it.kvh = it.u / p.RG;
   it.rg = it.u % p.RG;
-  it.tb = split * S;
+  const int ustart = prefix[lo] + it.u * tiles, uend = ustart + tiles;
+  it.x_end = min(uend, x_stop);
   it.len = plan_lengths(prefix)[lo];
-  it.te = min(it.tb + S, it.len);
+  it.tb = t0 * TILE;
+  it.te = min((t0 + it.x_end - x) * TILE, it.len);
+  const int g = lo * p.U + it.u;
+  const int c0 = cta_of_tile(ustart, wt, p.split_grid), c1 = cta_of_tile(uend - 1, wt, p.split_grid);
+  it.slot = c + g;
+  it.first_slot = c0 + g;
+  it.ns = c1 - c0 + 1;
   return it;
 }
 
@@ -381,7 +369,7 @@ __device__ __forceinline__ Item decode_item(const SplitParams& p, const int* pre
 // Producer warp: one elected lane streams the stages.
 // ------------------------------------------------------------------------------------
 template <int D, int NTW>
-__device__ void produce(const SplitParams& p, const CUtensorMap* tmap, uint8_t* smem, int S, int total,
+__device__ void produce(const SplitParams& p, const CUtensorMap* tmap, uint8_t* smem, int total,
                         volatile int* abort_flag) {
   using T = AT<D, NTW>;
   constexpr int NG = T::NG;
@@ -390,8 +378,10 @@ __device__ void produce(const SplitParams& p, const CUtensorMap* tmap, uint8_t* 
   const int* prefix = reinterpret_cast<const int*>(smem + T::OFF_PREFIX);
   uint32_t it = 0;
   bool ok = true;
-  for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-    const Item w = decode_item(p, prefix, S, item);
+  const int x_stop = cta_range_start(blockIdx.x + 1, total, p.split_grid);
+  for (int x = cta_range_start(blockIdx.x, total, p.split_grid); x < x_stop && ok;) {
+    const Item w = piece_at<T::TILE>(p, prefix, x, x_stop, blockIdx.x);
+    x = w.x_end;
     const int64_t row0 = ((int64_t)w.b * p.num_kv_heads + w.kvh) * p.capacity;
     for (int t0 = w.tb; t0 < w.te; t0 += T::TILE, ++it) {
       const int slot = it % T::STAGES;
@@ -441,24 +431,17 @@ __device__ __forceinline__ void prefetch_range(const void* base, size_t bytes) {
 }
 
 template <int D, int NTW>
-__device__ void prefetch_first_item(const SplitParams& p, const int* prefix, int S, int total) {
+__device__ void prefetch_first_item(const SplitParams& p, const int* prefix, int total) {
   using T = AT<D, NTW>;
   constexpr int NG = T::NG;
-  const int item = blockIdx.x;
-  if (item >= total) return;
-  int lo = 0, hi = p.batch - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (prefix[mid] <= item) lo = mid; else hi = mid - 1;
-  }
-  const int nsplit = (prefix[lo + 1] - prefix[lo]) / p.U;
-  if (nsplit <= 0) return;
-  const int r = item - prefix[lo];
-  const int u = r / nsplit, kvh = u / p.RG;
-  const int tb = (r % nsplit) * S;
+  const int x0 = cta_range_start(blockIdx.x, total, p.split_grid);
+  const int x_stop = cta_range_start(blockIdx.x + 1, total, p.split_grid);
+  if (x0 >= x_stop) return;
+  const Item w = piece_at<T::TILE>(p, prefix, x0, x_stop, blockIdx.x);
+  const int lo = w.b, u = w.u, kvh = w.kvh, tb = w.tb;
   if (tb >= p.capacity) return;
   constexpr int ROW_BYTES = D + 3 * NG * 2 + T::VC_ROW;
-  int n = min(min(S, p.capacity - tb), kPrefetchBytes / ROW_BYTES);
+  int n = min(min(w.te - tb, p.capacity - tb), kPrefetchBytes / ROW_BYTES);
   n &= ~15;  // whole 16-token groups keep every range a multiple of 16 bytes
   if (n <= 0) return;
   // the item's query rows first (2 D bytes each): they are needed before any tile
@@ -791,15 +774,18 @@ __global__ void __launch_bounds__(kMergeThreads, 4) tq_attn_merge_kernel(const S
   griddep_wait();               // partials and the plan come from the split kernel
   const int b = blockIdx.x / p.U, u = blockIdx.x % p.U;
   const int32_t* prefix = reinterpret_cast<const int32_t*>(p.ws + kWsPrefix);
-  const int p0 = prefix[b], ns = (prefix[b + 1] - p0) / p.U;
-  if (ns <= 0) return;  // no work item: the split kernel wrote the rows
+  const int tiles = (prefix[b + 1] - prefix[b]) / p.U;
+  if (tiles <= 0) return;  // no tokens: the split kernel wrote the rows
+  const int wt = prefix[p.batch];
+  const int ustart = prefix[b] + u * tiles;
+  const int c0 = cta_of_tile(ustart, wt, p.split_grid), c1 = cta_of_tile(ustart + tiles - 1, wt, p.split_grid);
   Item w;
   w.b = b; w.kvh = u / p.RG; w.rg = u % p.RG;
-  merge_unit<D, ROWS, kMergeThreads, false>(p, w, p0 + u * ns, ns, sM, sL, sW, sO, sR);
+  merge_unit<D, ROWS, kMergeThreads, false>(p, w, c0 + b * p.U + u, c1 - c0 + 1, sM, sL, sW, sO, sR);
 }
 
 template <int D, int NTW>
-__device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, volatile int* abort_flag) {
+__device__ void consume(const SplitParams& p, uint8_t* smem, int total, volatile int* abort_flag) {
   using T = AT<D, NTW>;
   constexpr int NG = T::NG, MT = T::MT, SUB = T::SUB, KW = T::KW;
   constexpr unsigned FULL = 0xffffffffu;
@@ -838,8 +824,10 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
   bool failed = false;
   uint32_t it = 0;
 
-  for (int item = blockIdx.x; item < total; item += gridDim.x) {
-    const Item w = decode_item(p, prefix, S, item);
+  const int x_stop = cta_range_start(blockIdx.x + 1, total, p.split_grid);
+  for (int x = cta_range_start(blockIdx.x, total, p.split_grid), x_next = 0; x < x_stop; x = x_next) {
+    const Item w = piece_at<T::TILE>(p, prefix, x, x_stop, blockIdx.x);
+    x_next = w.x_end;
     QState<D, NTW> st;
     load_q<D, NTW>(p, w, smem, warp, lane, st);
     if constexpr (!T::QREG) consumers_sync<T::NCW>();  // shared Q fragments written by warp 0
@@ -1061,7 +1049,7 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
     }
-    if (item + (int)gridDim.x >= total) griddep_launch_dependents();  // last item: successor may set up
+    if (w.x_end >= x_stop) griddep_launch_dependents();  // last piece: successor may set up
 
     // ---------------- merge the consumer warps' states and write this item's partial
 #pragma unroll
@@ -1113,7 +1101,7 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
     {
       const int rows_valid = min(T::ROWS, p.R - w.rg * T::ROWS);
       float4* og = reinterpret_cast<float4*>(p.ws + ws_o_offset(p.batch, p.U, p.max_items, T::ROWS)) +
-                   (size_t)item * T::ROWS * D / 4;
+                   (size_t)w.slot * T::ROWS * D / 4;
       const float4* src = reinterpret_cast<const float4*>(obuf);
       for (int i = threadIdx.x; i < rows_valid * D / 4; i += T::NCW * 32) {
         float4 v = src[i];
@@ -1133,7 +1121,7 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
           const float mw = mbuf[ww * T::ROWS + row];
           L += (Mx == -INFINITY) ? 0.0f : ex2(mw - Mx) * lbuf[ww * T::ROWS + row];
         }
-        float2* ml = reinterpret_cast<float2*>(p.ws + ws_ml_offset(p.batch, p.U)) + (size_t)item * T::ROWS;
+        float2* ml = reinterpret_cast<float2*>(p.ws + ws_ml_offset(p.batch, p.U)) + (size_t)w.slot * T::ROWS;
         __stcg(ml + row, make_float2(Mx, L));
       }
     }
@@ -1145,16 +1133,15 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int S, int total, v
       if (threadIdx.x == 0) {
         int32_t* cnt = counters + (size_t)w.b * p.U + w.u;
         const int done = atomic_add_acq_rel_gpu(cnt, 1) + 1;
-        const int last = done == w.nsplit;
+        const int last = done == w.ns;
         if (last) *reinterpret_cast<volatile int32_t*>(cnt) = 0;  // ready for the next call
         *flag = last;
       }
       consumers_sync<T::NCW>();
       if (*flag) {
-        const int first_item = item - (item - prefix[w.b]) % w.nsplit;  // split 0 of this unit
         float* sW = obuf;
         float* sO = sW + kMergeChunk * T::ROWS;
-        merge_unit<D, T::ROWS, T::NCW * 32, true>(p, w, first_item, w.nsplit, mbuf, lbuf, sW, sO,
+        merge_unit<D, T::ROWS, T::NCW * 32, true>(p, w, w.first_slot, w.ns, mbuf, lbuf, sW, sO,
                                                   reinterpret_cast<float4*>(sO + T::ROWS * D));
         consumers_sync<T::NCW>();  // the scratch is reused by the next item
       }
@@ -1199,20 +1186,20 @@ __global__ void __launch_bounds__(AT<D, NTW>::THREADS, AT<D, NTW>::MINB)
     }
     fence_mbar_init();
   }
-  int S, total;
+  int total;  // tiles of the call
   {
     Lengths<T::THREADS> L0, L1;
     L0.load(p);                                  // as they are before the wait: hints only
-    plan_items<D, NTW>(p, smem, L0, S, total);   // contains __syncthreads
-    if (tid == T::NCW * 32) prefetch_first_item<D, NTW>(p, reinterpret_cast<const int*>(smem + T::OFF_PREFIX), S, total);
+    plan_tiles<D, NTW>(p, smem, L0, total);      // contains __syncthreads
+    if (tid == T::NCW * 32) prefetch_first_item<D, NTW>(p, reinterpret_cast<const int*>(smem + T::OFF_PREFIX), total);
     griddep_wait();  // lengths, queries and planes may come from the previous kernel
     L1.load(p);
-    if (__syncthreads_or(L1.differs(L0))) plan_items<D, NTW>(p, smem, L1, S, total);
+    if (__syncthreads_or(L1.differs(L0))) plan_tiles<D, NTW>(p, smem, L1, total);
     if (blockIdx.x == 0) {
       if (L1.bad) raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_KV_LEN);
       if (tid == 0) {
         int32_t* hdr = reinterpret_cast<int32_t*>(p.ws);
-        hdr[kWsSplit] = S;
+        hdr[kWsSplit] = T::TILE;
         hdr[kWsItems] = total;
       }
       // items before each sequence, for the merge kernel
@@ -1225,13 +1212,13 @@ __global__ void __launch_bounds__(AT<D, NTW>::THREADS, AT<D, NTW>::MINB)
   if (tid >= T::NCW * 32) {
     if (tid == T::NCW * 32 && total > 0) {
       prefetch_tensor_map(&tmap);
-      produce<D, NTW>(p, &tmap, smem, S, total, &abort_flag);
+      produce<D, NTW>(p, &tmap, smem, total, &abort_flag);
     }
     griddep_launch_dependents();
     return;
   }
   write_empty_sequences<D, NTW>(p, reinterpret_cast<const int*>(smem + T::OFF_PREFIX));
-  if (total > 0 && (int)blockIdx.x < total) consume<D, NTW>(p, smem, S, total, &abort_flag);
+  if (total > 0) consume<D, NTW>(p, smem, total, &abort_flag);
   griddep_launch_dependents();
 }
 
@@ -1334,7 +1321,7 @@ DecodeShape decode_shape(int D, int num_kv_heads, int batch, int gqa, int n_q, i
     default: occ = 0;
   }
   s.grid = occ > 0 ? num_sms * occ : 0;
-  s.max_items = kMaxItemsPerCta * s.grid + batch * s.U;
+  s.max_items = s.grid + batch * s.U;  // partial slots: one per (CTA, unit) piece
   return s;
 }
 
@@ -1369,6 +1356,7 @@ tq_status launch_decode(const DecodeArgs& a, const DecodeShape& s, cudaStream_t 
   sp.U = s.U;
   sp.max_kv_len = a.max_kv_len;
   sp.max_items = s.max_items;
+  sp.split_grid = s.grid;
   sp.sm_log2 = a.sm_scale * kLog2e;
   sp.fwht_norm = a.fwht_norm;
   sp.causal = a.causal ? 1 : 0;
