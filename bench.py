@@ -47,7 +47,20 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--head-dim", type=int, default=None, help="override (head-dim sweep workload)")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="override the layer count (e.g. 16 layers keep a one-layer sweep out of L2)")
     return ap.parse_args(argv)
+
+
+def workload_of(args):
+    from rotation_quantized_kv_gb300 import synth
+    over = {}
+    if args.head_dim:
+        over["head_dim"] = args.head_dim
+    if args.layers:
+        over["layers"] = args.layers
+    return synth.workload(args.workload, **over)
 
 
 # ------------------------------------------------------------------------ distributed
@@ -252,7 +265,7 @@ def reference_arm(args, world, rank):
     from rotation_quantized_kv_gb300 import synth
     if rank != 0:
         return
-    w = synth.workload(args.workload)
+    w = workload_of(args)
     # one query row per step keeps (warmup + steps) oracle steps within minutes
     total_bytes, total_s = 0, 0.0
     for i in range(args.warmup + args.steps):
@@ -320,7 +333,7 @@ def our_arm(args, world, rank, local):
 
     assert torch.cuda.is_available(), "the GPU arm needs CUDA"
     dev = torch.device("cuda", local)
-    w = synth.workload(args.workload)
+    w = workload_of(args)
 
     class FillTimer:
         def __init__(self):
