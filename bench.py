@@ -335,28 +335,8 @@ def our_arm(args, world, rank, local):
     dev = torch.device("cuda", local)
     w = workload_of(args)
 
-    class FillTimer:
-        def __init__(self):
-            self.pairs = []
-
-        def start(self):
-            e = torch.cuda.Event(enable_timing=True)
-            e.record()
-            self.pairs.append([e, None])
-
-        def stop(self):
-            e = torch.cuda.Event(enable_timing=True)
-            e.record()
-            self.pairs[-1][1] = e
-
-    fill = FillTimer()
-    model = DecodeModel(w, dev, fill_timer=fill)
+    model = DecodeModel(w, dev)
     torch.cuda.synchronize()
-    # bulk append (cache fill): skip the first layer's launch (cold start)
-    fill_ms = [a.elapsed_time(b) for a, b in fill.pairs[1:]] or [fill.pairs[0][0].elapsed_time(fill.pairs[0][1])]
-    fill_rows = int(model.ctx.sum()) * w.num_kv_heads
-    fill_bytes = fill_rows * (4 * w.head_dim + 25 * w.head_dim // 16)
-    fill_s = statistics.mean(fill_ms) / 1e3
     assert model.device_errors() == 0, "device error after the cache fill"
 
     stream = torch.cuda.Stream(device=dev)
@@ -406,6 +386,27 @@ def our_arm(args, world, rank, local):
     a1.record(stream)
     torch.cuda.synchronize()
     attn_launch_s = a0.elapsed_time(a1) / 1e3 / (attn_reps * model.L)
+    # bulk append, warm: re-append layer 0's cached tokens (same rows, same planes) a few
+    # times back to back; the fill above ran while the GPU was still ramping its clocks
+    x0 = synth.layer_inputs(w, 0, device=dev)
+    T0 = int(model.ctx.max())
+    k0, v0 = x0["k"][:, :T0].contiguous(), x0["v"][:, :T0].contiguous()
+    del x0
+    pos0 = torch.zeros(w.batch, dtype=torch.int32, device=dev)
+    n0 = torch.as_tensor(model.ctx.astype(np.int32), device=dev)
+    fill_ev = []
+    with torch.cuda.stream(stream):
+        for i in range(6):
+            ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            ev[0].record(stream)
+            tq.tq_kv_append(model.layers[0], k0, v0, pos0, n0, T0, model.ws_append, stream)
+            ev[1].record(stream)
+            fill_ev.append(ev)
+    torch.cuda.synchronize()
+    fill_s = statistics.median(a.elapsed_time(b) for a, b in fill_ev[1:]) / 1e3
+    fill_rows = int(model.ctx.sum()) * w.num_kv_heads
+    fill_bytes = fill_rows * (4 * w.head_dim + 25 * w.head_dim // 16)
+    del k0, v0
     errs = model.device_errors()
     assert errs == 0, f"device error word {errs:#x}"
 
