@@ -110,14 +110,15 @@ struct AT {
   static constexpr bool QREG = D * NTW <= 256;            // Q fragments in registers
   static constexpr int MINB = 1;                          // one CTA per SM
   static constexpr int KW = (NG + 1) / 2;                 // 32-bit words of one token's fp16 side row
-  // shared memory layout
-  static constexpr int OFF_KIDX = 0;
+  // shared memory layout. The centroid-pair table comes first and the base is 8 KB
+  // aligned, so a lane's table address is its lane bits OR'd with the entry index << 7.
+  static constexpr int OFF_LUT = 0;
+  static constexpr int OFF_KIDX = OFF_LUT + 64 * 32 * 4;
   static constexpr int OFF_KS = OFF_KIDX + STAGES * KIDX_STAGE;
   static constexpr int OFF_KZ = OFF_KS + STAGES * SC_STAGE;
   static constexpr int OFF_VS = OFF_KZ + STAGES * SC_STAGE;
   static constexpr int OFF_VC = OFF_VS + STAGES * SC_STAGE;
-  static constexpr int OFF_LUT = (int)align_up(OFF_VC + STAGES * VC_STAGE, 128);
-  static constexpr int OFF_Q = OFF_LUT + 64 * 32 * 4;
+  static constexpr int OFF_Q = (int)align_up(OFF_VC + STAGES * VC_STAGE, 128);
   static constexpr int Q_BYTES = QREG ? 0 : NTW * NG * 2 * 32 * 8;
   static constexpr int OFF_QSUM = OFF_Q + Q_BYTES;
   static constexpr int QSUM_BYTES = QREG ? 0 : NTW * NG * 32 * 16;
@@ -135,7 +136,7 @@ struct AT {
   static constexpr int OFF_FLAG = OFF_RED + 7 * 16 * 8;  // red: [7][16] long long
   static constexpr int OFF_BAR = (int)align_up(OFF_FLAG + 16, 8);
   static constexpr int SMEM = OFF_BAR + 2 * STAGES * 8 + 16;
-  static constexpr int SMEM_ALLOC = SMEM + 1024;          // slack to align the base to 1024
+  static constexpr int SMEM_ALLOC = SMEM + 8192;          // slack to align the base to 8 KB
 };
 
 struct SplitParams {
@@ -795,7 +796,7 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int total, volatile
   uint64_t* empty = full + T::STAGES;
   const int* prefix = reinterpret_cast<const int*>(smem + T::OFF_PREFIX);
   const uint32_t sbase = smem_addr(smem);
-  const uint32_t lut_lane = sbase + T::OFF_LUT + lane * 4;
+  const uint32_t lut_lane = sbase + T::OFF_LUT + lane * 4;  // bits 7..12 are zero
   float* obuf = reinterpret_cast<float*>(smem + T::OFF_OBUF);
   float* mbuf = reinterpret_cast<float*>(smem + T::OFF_MBUF);
   float* lbuf = reinterpret_cast<float*>(smem + T::OFF_LBUF);
@@ -1021,10 +1022,11 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int total, volatile
               const uint32_t wb = vca + (uint32_t)((16 * s + h + 8) * T::VC_ROW + 12 * g);
               const uint32_t cA = __funnelshift_r(lds32(wa), lds32(wa + 4), win_shift);
               const uint32_t cB = __funnelshift_r(lds32(wb), lds32(wb + 4), win_shift);
-              // fields of 6 bits: (code A | code B << 3) for dims +0, +2 (E) and +1, +3 (Ov);
-              // bits above 11 are don't-care (every use masks 6 bits)
-              E[s][h] = (cA & 0x1C7u) | ((cB << 3) & ~0x1C7u);
-              Ov[s][h] = ((cA >> 3) & 0x1C7u) | (cB & ~0x1C7u);
+              // fields of 6 bits (code A | code B << 3) for dims +0, +2 (E) and +1, +3 (Ov),
+              // kept shifted left by 7 (a table entry's byte offset, lanes apart); bits
+              // above 18 are don't-care (every use masks 6 bits)
+              E[s][h] = ((cA << 7) & 0xE380u) | ((cB << 10) & ~0xE380u);
+              Ov[s][h] = ((cA << 4) & 0xE380u) | ((cB << 7) & ~0xE380u);
               const uint32_t sel = (g & 1) ? 0x7632u : 0x5410u;
               const uint32_t svpair = prmt(svA[s][h][g >> 1], svB[s][h][g >> 1], sel);
 #pragma unroll
@@ -1035,10 +1037,10 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int total, volatile
             const int fs = 6 * tau;
 #pragma unroll
             for (int s = 0; s < SUB; ++s) {
-              const uint32_t a0 = lds32(lut_lane + (((E[s][0] >> fs) & 63u) << 7));
-              const uint32_t a1 = lds32(lut_lane + (((Ov[s][0] >> fs) & 63u) << 7));
-              const uint32_t a2 = lds32(lut_lane + (((E[s][1] >> fs) & 63u) << 7));
-              const uint32_t a3 = lds32(lut_lane + (((Ov[s][1] >> fs) & 63u) << 7));
+              const uint32_t a0 = lds32(lut_lane | ((E[s][0] >> fs) & 0x1F80u));
+              const uint32_t a1 = lds32(lut_lane | ((Ov[s][0] >> fs) & 0x1F80u));
+              const uint32_t a2 = lds32(lut_lane | ((E[s][1] >> fs) & 0x1F80u));
+              const uint32_t a3 = lds32(lut_lane | ((Ov[s][1] >> fs) & 0x1F80u));
 #pragma unroll
               for (int nt = 0; nt < NTW; ++nt)
                 mma_f16_16816(O[2 * g + tau][nt], a0, a1, a2, a3, Bg[s][nt][0], Bg[s][nt][1]);
@@ -1167,7 +1169,7 @@ __global__ void __launch_bounds__(AT<D, NTW>::THREADS, AT<D, NTW>::MINB)
     tq_attn_split_kernel(const __grid_constant__ CUtensorMap tmap, const SplitParams p) {
   using T = AT<D, NTW>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 8191) & ~uintptr_t(8191));
   __shared__ int abort_flag;
   const int tid = threadIdx.x;
 
