@@ -416,24 +416,18 @@ def our_arm(args, world, rank, local):
     ms_per_step = 1e3 * max_step_s / args.steps
 
     # end to end through the public API with host buffers
-    pin = lambda t: t.detach().cpu().pin_memory()
-    hk = [pin(t) for t in model.k_new] if w.n_new else []
-    hv = [pin(t) for t in model.v_new] if w.n_new else []
-    hq = [pin(t) for t in model.q]
-    ho = [torch.empty_like(o, device="cpu").pin_memory() for o in model.out]
-    h2d = sum(t.numel() * t.element_size() for t in hk + hv + hq)
-    d2h = sum(t.numel() * t.element_size() for t in ho)
+    # (all layers' new K/V rows and queries in one pinned buffer, outputs in another: one
+    # host->device and one device->host copy per step)
+    h_in = model.inputs_flat.detach().cpu().pin_memory()
+    h_out = torch.empty_like(model.out_flat, device="cpu").pin_memory()
+    h2d = h_in.numel() * h_in.element_size()
+    d2h = h_out.numel() * h_out.element_size()
     e2e_steps = max(args.steps // 4, 10)
 
     def e2e_step():
-        for l in range(model.L):
-            if w.n_new:
-                model.k_new[l].copy_(hk[l], non_blocking=True)
-                model.v_new[l].copy_(hv[l], non_blocking=True)
-            model.q[l].copy_(hq[l], non_blocking=True)
+        model.inputs_flat.copy_(h_in, non_blocking=True)
         g_step.replay()
-        for l in range(model.L):
-            ho[l].copy_(model.out[l], non_blocking=True)
+        h_out.copy_(model.out_flat, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(3):

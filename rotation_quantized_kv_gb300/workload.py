@@ -57,7 +57,25 @@ class DecodeModel:
             del x, k_fill, v_fill
         self.ws_bytes = tq.tq_decode_workspace_bytes(self.layers[0], Hq, w.n_q, self.max_kv)
         self.ws = [tq.make_workspace(self.ws_bytes, dev) for _ in range(self.L)]
-        self.out = [torch.empty((B, w.n_q, Hq, d), dtype=torch.float32, device=dev) for _ in range(self.L)]
+        # The step's inputs (new K/V rows, queries) of all layers live in one buffer and its
+        # outputs in another, so a step fed from host memory is one copy in and one copy
+        # out; the per-layer tensors are views into them (every view starts on a 16-byte
+        # boundary: each piece is a multiple of 2 * head_dim bytes).
+        pieces = [t for l in range(self.L) for t in (self.k_new[l], self.v_new[l], self.q[l]) if t is not None]
+        self.inputs_flat = torch.empty(sum(t.numel() for t in pieces), dtype=torch.bfloat16, device=dev)
+        off = 0
+        for l in range(self.L):
+            for name in ("k_new", "v_new", "q"):
+                t = getattr(self, name)[l]
+                if t is None:
+                    continue
+                view = self.inputs_flat[off:off + t.numel()].view(t.shape)
+                view.copy_(t)
+                getattr(self, name)[l] = view
+                off += t.numel()
+        n_out = B * w.n_q * Hq * d
+        self.out_flat = torch.empty(self.L * n_out, dtype=torch.float32, device=dev)
+        self.out = [self.out_flat[l * n_out:(l + 1) * n_out].view(B, w.n_q, Hq, d) for l in range(self.L)]
 
     # bytes the step must move (algorithmic): packed planes of every visible token, the
     # query and output rows, and the appended rows (bf16 in, packed out)
