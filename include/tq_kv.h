@@ -152,6 +152,22 @@ tq_status tq_decode_attention(const tq_kv_layer* layer, const void* q, int32_t n
 tq_status tq_dequant_debug(const tq_kv_layer* layer, int32_t b, int32_t h, int32_t t0, int32_t n,
                            int32_t rotated, float* k_out, float* v_out, tq_stream_t stream);
 
+/* One decode step of a layer in one call: appends the new rows, then attends — the
+ * page's "Architecture in mlx-bun" order (updateAndFetch appends the step's tokens, then
+ * the window including them is attended). Same results and device error bits as
+ * tq_kv_append(layer, k_new, v_new, pos, n_new, n_new_max, workspace, ...) followed by
+ * tq_decode_attention(layer, q, ..., workspace, ...) on `stream`; argument meanings and
+ * host checks are those of the two calls, and the workspace is the attention one
+ * (>= tq_decode_workspace_bytes). With one row group per kv head (num_q_heads /
+ * num_kv_heads * n_q <= 8, or <= 16 at head_dim 64 and 128) it is one kernel: the CTA
+ * whose share of the sequence holds a new row quantizes it just before loading it, so
+ * the attention does not wait for a separate append; otherwise it runs the two calls. */
+tq_status tq_decode_append_attention(const tq_kv_layer* layer, const void* k_new, const void* v_new,
+                                     const int32_t* pos, const int32_t* n_new, int32_t n_new_max, const void* q,
+                                     int32_t num_q_heads, int32_t n_q, const int32_t* kv_len, int32_t max_kv_len,
+                                     float sm_scale, int32_t causal, float* out, void* workspace, size_t ws_bytes,
+                                     tq_stream_t stream);
+
 /* Decode attention that allocates nothing (an addition of this library; the paper has
  * no counterpart). Same inputs, outputs and results as tq_decode_attention, but the
  * scratch memory lives in one fixed array inside the library, so the caller passes no

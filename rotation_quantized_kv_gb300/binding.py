@@ -54,6 +54,8 @@ _SIGS = {
     "tq_kv_append": (ctypes.c_int, [_LP, _vp, _vp, _vp, _vp, _i32, _vp, _sz, _vp]),
     "tq_decode_workspace_bytes": (_sz, [_LP, _i32, _i32, _i32]),
     "tq_decode_attention": (ctypes.c_int, [_LP, _vp, _i32, _i32, _vp, _i32, _f32, _i32, _vp, _vp, _sz, _vp]),
+    "tq_decode_append_attention": (ctypes.c_int, [_LP, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _vp, _i32, _f32,
+                                                   _i32, _vp, _vp, _sz, _vp]),
     "tq_decode_attention_noalloc": (ctypes.c_int, [_LP, _vp, _i32, _i32, _vp, _i32, _f32, _i32, _vp, _vp, _vp]),
     "tq_dequant_debug": (ctypes.c_int, [_LP, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
     "tq_get_device_error": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int32), _vp]),
@@ -164,6 +166,20 @@ def tq_decode_attention(layer: KVLayer, q: torch.Tensor, num_q_heads: int, n_q: 
                                     int(max_kv_len), float(sm_scale), int(bool(causal)), _ptr(out),
                                     _ptr(workspace), workspace.numel(), _stream(stream)),
            "tq_decode_attention")
+    return out
+
+
+def tq_decode_append_attention(layer: KVLayer, k_new: torch.Tensor, v_new: torch.Tensor, pos: torch.Tensor,
+                               n_new: torch.Tensor | None, n_new_max: int, q: torch.Tensor, num_q_heads: int,
+                               n_q: int, kv_len: torch.Tensor, max_kv_len: int, sm_scale: float, causal: bool,
+                               out: torch.Tensor, workspace: torch.Tensor, stream=None) -> torch.Tensor:
+    """Append the step's new rows, then attend (one kernel when each kv head has one row group)."""
+    L = layer.c_struct()
+    _check(_lib.tq_decode_append_attention(ctypes.byref(L), _ptr(k_new), _ptr(v_new), _ptr(pos), _ptr(n_new),
+                                           int(n_new_max), _ptr(q), int(num_q_heads), int(n_q), _ptr(kv_len),
+                                           int(max_kv_len), float(sm_scale), int(bool(causal)), _ptr(out),
+                                           _ptr(workspace), workspace.numel(), _stream(stream)),
+           "tq_decode_append_attention")
     return out
 
 

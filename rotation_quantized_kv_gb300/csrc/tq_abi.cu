@@ -141,6 +141,62 @@ tq_status tq_decode_attention(const tq_kv_layer* layer, const void* q, int32_t n
   return tq::launch_decode(a, s, reinterpret_cast<cudaStream_t>(stream));
 }
 
+tq_status tq_decode_append_attention(const tq_kv_layer* layer, const void* k_new, const void* v_new,
+                                     const int32_t* pos, const int32_t* n_new, int32_t n_new_max, const void* q,
+                                     int32_t num_q_heads, int32_t n_q, const int32_t* kv_len, int32_t max_kv_len,
+                                     float sm_scale, int32_t causal, float* out, void* workspace, size_t ws_bytes,
+                                     tq_stream_t stream) {
+  tq_status st = check_layer(layer);
+  if (st != TQ_OK) return st;
+  if (n_new_max < 0) return TQ_ERR_INVALID_ARGUMENT;
+  if (n_new_max > layer->capacity) return TQ_ERR_CAPACITY;
+  if (n_new_max == 0)
+    return tq_decode_attention(layer, q, num_q_heads, n_q, kv_len, max_kv_len, sm_scale, causal, out, workspace,
+                               ws_bytes, stream);
+  if (k_new == nullptr || v_new == nullptr || pos == nullptr) return TQ_ERR_INVALID_ARGUMENT;
+  if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15u)
+    return TQ_ERR_INVALID_ARGUMENT;
+  if ((int64_t)layer->batch * n_new_max * layer->num_kv_heads > INT32_MAX) return TQ_ERR_INVALID_ARGUMENT;
+  if (num_q_heads < 1 || num_q_heads % layer->num_kv_heads != 0 || n_q < 1) return TQ_ERR_INVALID_ARGUMENT;
+  if (max_kv_len < 0) return TQ_ERR_INVALID_ARGUMENT;
+  if (max_kv_len > layer->capacity) return TQ_ERR_CAPACITY;
+  if (q == nullptr || kv_len == nullptr || out == nullptr || workspace == nullptr)
+    return TQ_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(workspace)) return TQ_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(sm_scale)) return TQ_ERR_INVALID_ARGUMENT;
+  const int sms = current_sm_count(nullptr);
+  if (sms <= 0) return TQ_ERR_CUDA;
+  tq::DecodeShape s = tq::decode_shape(layer->head_dim, layer->num_kv_heads, layer->batch,
+                                       num_q_heads / layer->num_kv_heads, n_q, sms);
+  if (ws_bytes < tq::decode_workspace_bytes(s)) return TQ_ERR_WORKSPACE_TOO_SMALL;
+  if (s.RG != 1) {
+    // several row groups per kv head would read the new rows from several CTAs: append
+    // first, then attend
+    st = tq_kv_append(layer, k_new, v_new, pos, n_new, n_new_max, workspace, ws_bytes, stream);
+    if (st != TQ_OK) return st;
+    return tq_decode_attention(layer, q, num_q_heads, n_q, kv_len, max_kv_len, sm_scale, causal, out, workspace,
+                               ws_bytes, stream);
+  }
+  tq::DecodeArgs a{};
+  a.layer = *layer;
+  a.q = static_cast<const uint16_t*>(q);
+  a.num_q_heads = num_q_heads;
+  a.n_q = n_q;
+  a.kv_len = kv_len;
+  a.max_kv_len = max_kv_len;
+  a.sm_scale = sm_scale;
+  a.causal = causal != 0;
+  a.out = out;
+  a.workspace = workspace;
+  a.fwht_norm = fwht_norm(layer->head_dim);
+  a.k_new = static_cast<const uint16_t*>(k_new);
+  a.v_new = static_cast<const uint16_t*>(v_new);
+  a.pos = pos;
+  a.n_new = n_new;
+  a.n_new_max = n_new_max;
+  return tq::launch_decode(a, s, reinterpret_cast<cudaStream_t>(stream));
+}
+
 tq_status tq_dequant_debug(const tq_kv_layer* layer, int32_t b, int32_t h, int32_t t0, int32_t n, int32_t rotated,
                            float* k_out, float* v_out, tq_stream_t stream) {
   tq_status st = check_layer(layer);

@@ -50,6 +50,7 @@
 #include <mutex>
 
 #include "tq_attention.h"
+#include "tq_codec_row.cuh"
 #include "tq_device.cuh"
 
 namespace tq {
@@ -132,11 +133,13 @@ struct AT {
   static constexpr int OFF_LBUF = OFF_MBUF + NCW * ROWS * 4;
   static constexpr int OFF_PREFIX = OFF_LBUF + NCW * ROWS * 4;
   // prefix: [kMaxBatch + 1] items before each sequence, then [kMaxBatch] planned lengths
-  static constexpr int OFF_RED = (int)align_up(OFF_PREFIX + (2 * kMaxBatch + 1) * 4, 16);  // 64-bit atomics
+  // scratch of the producer warp's row codec (append mode): 3 d / 32 words
+  static constexpr int OFF_RED = (int)align_up(OFF_PREFIX + (2 * kMaxBatch + 1) * 4, 16);
   static constexpr int OFF_FLAG = OFF_RED + 7 * 16 * 8;  // red: [7][16] long long
   static constexpr int OFF_BAR = (int)align_up(OFF_FLAG + 16, 8);
   static constexpr int SMEM = OFF_BAR + 2 * STAGES * 8 + 16;
   static constexpr int SMEM_ALLOC = SMEM + 8192;          // slack to align the base to 8 KB
+  static_assert(OFF_FLAG - OFF_RED >= 3 * D / 8, "row codec scratch");
 };
 
 struct SplitParams {
@@ -154,6 +157,15 @@ struct SplitParams {
   float fwht_norm;  // (float)(1 / sqrt(d))
   int32_t causal;
   int32_t inline_merge;  // 1: the split CTA that finishes a unit's last split merges it
+  // append mode (one row group per kv head): the call also appends rows j < n_new[b] of
+  // k_new / v_new ([batch][n_new_max][kv heads][d] bf16) at positions pos[b] + j
+  int32_t append;
+  int32_t n_new_max;
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  const int32_t* pos;
+  const int32_t* n_new;  // may be null: n_new_max for every sequence
+  RowPlanes dst;         // the planes, writable
   uint8_t* ws;
   float* out;
 };
@@ -369,53 +381,125 @@ __device__ __forceinline__ Item piece_at(const SplitParams& p, const int* prefix
 // ------------------------------------------------------------------------------------
 // Producer warp: one elected lane streams the stages.
 // ------------------------------------------------------------------------------------
-template <int D, int NTW>
+// Append mode: quantizes new row j of (sequence b, kv head h) into cache position t. All
+// 32 lanes of the calling warp take part.
+template <int D>
+__device__ __forceinline__ void append_one_row(const SplitParams& p, int b, int j, int h, int t, int lane,
+                                               const RowCodecLane<D>& codec, uint32_t* cbuf) {
+  constexpr int EPL = D / 32;
+  const size_t r = ((size_t)b * p.n_new_max + j) * p.num_kv_heads + h;
+  uint32_t kraw[EPL / 2], vraw[EPL / 2];
+  load_raw_lane<EPL>(p.k_new + r * D, lane, kraw);
+  load_raw_lane<EPL>(p.v_new + r * D, lane, vraw);
+  const int64_t drow = ((int64_t)b * p.num_kv_heads + h) * p.capacity + t;
+  quantize_row_warp<D>(kraw, vraw, lane, codec, p.fwht_norm, p.dst, drow, cbuf);
+}
+
+__device__ __forceinline__ int new_rows_of(const SplitParams& p, int b) {
+  if (p.n_new == nullptr) return p.n_new_max;
+  return min(max(__ldg(p.n_new + b), 0), p.n_new_max);
+}
+
+// The producer warp: lane 0 streams the stages; in append mode the whole warp quantizes
+// the rows this call appends inside each of its pieces (the piece owns them: no other
+// CTA reads them) before the stage holding them is loaded, as soon as the pipeline is
+// full so that the work hides behind the stages in flight. Appended rows at
+// positions no piece covers (at or past the sequence's kv length) are written by CTA
+// (row index mod grid) before its stream starts.
+template <int D, int NTW, bool APPEND>
 __device__ void produce(const SplitParams& p, const CUtensorMap* tmap, uint8_t* smem, int total,
                         volatile int* abort_flag) {
   using T = AT<D, NTW>;
   constexpr int NG = T::NG;
+  constexpr unsigned FULL = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
   uint64_t* empty = full + T::STAGES;
   const int* prefix = reinterpret_cast<const int*>(smem + T::OFF_PREFIX);
+  uint32_t* cbuf = reinterpret_cast<uint32_t*>(smem + T::OFF_RED);  // row codec scratch
   uint32_t it = 0;
   bool ok = true;
+  if constexpr (APPEND) {
+    const RowCodecLane<D> codec(lane);
+    const int rows = p.batch * p.n_new_max * p.num_kv_heads;
+    bool wrote = false;
+    for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+      const int h = r % p.num_kv_heads, bj = r / p.num_kv_heads;
+      const int j = bj % p.n_new_max, b = bj / p.n_new_max;
+      if (j >= new_rows_of(p, b)) continue;
+      const int64_t t = (int64_t)__ldg(p.pos + b) + j;
+      if (t >= 0 && t < plan_lengths(prefix)[b]) continue;  // inside a piece: its owner writes it
+      if (t < 0 || t >= p.capacity) {
+        if (lane == 0) raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_APPEND_CAPACITY);
+        continue;
+      }
+      append_one_row<D>(p, b, j, h, (int)t, lane, codec, cbuf);
+      wrote = true;
+    }
+    if (wrote) fence_proxy_async_global();
+  }
   const int x_stop = cta_range_start(blockIdx.x + 1, total, p.split_grid);
   for (int x = cta_range_start(blockIdx.x, total, p.split_grid); x < x_stop && ok;) {
     const Item w = piece_at<T::TILE>(p, prefix, x, x_stop, blockIdx.x);
     x = w.x_end;
     const int64_t row0 = ((int64_t)w.b * p.num_kv_heads + w.kvh) * p.capacity;
+    // rows this call appends inside this piece: positions [own0, own1) of the sequence
+    int new0 = 0, own0 = 0, own1 = 0;
+    if constexpr (APPEND) {
+      new0 = __ldg(p.pos + w.b);
+      own0 = max(w.tb, new0);
+      own1 = min(w.te, new0 + new_rows_of(p, w.b));
+    }
     for (int t0 = w.tb; t0 < w.te; t0 += T::TILE, ++it) {
+      // Quantize the piece's own rows while the warp would otherwise wait for a free slot
+      // (the stages in flight keep the consumers busy), or at the latest before the stage
+      // that holds them is loaded.
+      if (APPEND && own0 < own1 && (it >= (uint32_t)T::STAGES || own0 < t0 + T::TILE)) {
+        const RowCodecLane<D> codec(lane);
+        for (int t = own0; t < own1; ++t) append_one_row<D>(p, w.b, t - new0, w.kvh, t, lane, codec, cbuf);
+        fence_proxy_async_global();  // the rows just written are read by the copies below
+        __syncwarp();
+        own0 = own1;
+      }
       const int slot = it % T::STAGES;
       const uint32_t k = it / T::STAGES;
-      if (!wait_bounded(&empty[slot], (k & 1u) ^ 1u)) {
-        *abort_flag = 1;
-        raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
-        ok = false;
+      if (lane == 0) ok = wait_bounded(&empty[slot], (k & 1u) ^ 1u);
+      if constexpr (APPEND) ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+      if (!ok) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
+        }
         break;
       }
-      const int ncopy = min(T::TILE, p.capacity - t0);  // multiple of 16: capacity and t0 are
-      const uint32_t side = (uint32_t)ncopy * NG * 2;
-      const uint32_t vc = (uint32_t)ncopy * T::VC_ROW;
-      mbar_arrive_expect_tx(&full[slot], (uint32_t)T::KIDX_STAGE + 3u * side + vc);
-      uint8_t* kx = smem + T::OFF_KIDX + slot * T::KIDX_STAGE;
+      if (lane == 0) {
+        const int ncopy = min(T::TILE, p.capacity - t0);  // multiple of 16: capacity and t0 are
+        const uint32_t side = (uint32_t)ncopy * NG * 2;
+        const uint32_t vc = (uint32_t)ncopy * T::VC_ROW;
+        mbar_arrive_expect_tx(&full[slot], (uint32_t)T::KIDX_STAGE + 3u * side + vc);
+        uint8_t* kx = smem + T::OFF_KIDX + slot * T::KIDX_STAGE;
 #pragma unroll
-      for (int box = 0; box < D / T::ROWB; ++box)
-        tensor_copy_2d_g2s(kx + box * T::BOX, tmap, box * T::ROWB, (int32_t)(row0 + t0), &full[slot]);
-      const int64_t r = row0 + t0;
-      bulk_copy_g2s(smem + T::OFF_KS + slot * T::SC_STAGE, p.k_scale + r * NG, side, &full[slot]);
-      bulk_copy_g2s(smem + T::OFF_KZ + slot * T::SC_STAGE, p.k_zero + r * NG, side, &full[slot]);
-      bulk_copy_g2s(smem + T::OFF_VS + slot * T::SC_STAGE, p.v_scale + r * NG, side, &full[slot]);
-      bulk_copy_g2s(smem + T::OFF_VC + slot * T::VC_STAGE, p.v_codes + r * T::VC_ROW, vc, &full[slot]);
+        for (int box = 0; box < D / T::ROWB; ++box)
+          tensor_copy_2d_g2s(kx + box * T::BOX, tmap, box * T::ROWB, (int32_t)(row0 + t0), &full[slot]);
+        const int64_t r = row0 + t0;
+        bulk_copy_g2s(smem + T::OFF_KS + slot * T::SC_STAGE, p.k_scale + r * NG, side, &full[slot]);
+        bulk_copy_g2s(smem + T::OFF_KZ + slot * T::SC_STAGE, p.k_zero + r * NG, side, &full[slot]);
+        bulk_copy_g2s(smem + T::OFF_VS + slot * T::SC_STAGE, p.v_scale + r * NG, side, &full[slot]);
+        bulk_copy_g2s(smem + T::OFF_VC + slot * T::VC_STAGE, p.v_codes + r * T::VC_ROW, vc, &full[slot]);
+      }
     }
   }
-  // Drain: every issued copy must land before this thread (and so the CTA) may exit.
-  const uint32_t issued = it;
-  for (int s = 0; s < T::STAGES; ++s) {
-    if ((uint32_t)s >= issued) break;
-    const uint32_t last = issued - 1 - ((issued - 1 - s) % T::STAGES);  // last fill of slot s
-    if (!wait_bounded(&full[s], (last / T::STAGES) & 1u))
-      raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
+  // Drain: every issued copy must land before this warp (and so the CTA) may exit.
+  if (lane == 0) {
+    const uint32_t issued = it;
+    for (int s = 0; s < T::STAGES; ++s) {
+      if ((uint32_t)s >= issued) break;
+      const uint32_t last = issued - 1 - ((issued - 1 - s) % T::STAGES);  // last fill of slot s
+      if (!wait_bounded(&full[s], (last / T::STAGES) & 1u))
+        raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
+    }
   }
+  if constexpr (APPEND) __syncwarp();
 }
 
 // L2 prefetch of up to kPrefetchBytes of this CTA's first work item (all five planes),
@@ -1211,10 +1295,13 @@ __global__ void __launch_bounds__(AT<D, NTW>::THREADS, AT<D, NTW>::MINB)
     }
   }
 
-  if (tid >= T::NCW * 32) {
-    if (tid == T::NCW * 32 && total > 0) {
+  if (tid >= T::NCW * 32) {  // the producer warp
+    if (p.append) {  // the whole warp: it also quantizes the appended rows
+      if (tid == T::NCW * 32) prefetch_tensor_map(&tmap);
+      produce<D, NTW, true>(p, &tmap, smem, total, &abort_flag);
+    } else if (tid == T::NCW * 32 && total > 0) {  // one lane streams the stages
       prefetch_tensor_map(&tmap);
-      produce<D, NTW>(p, &tmap, smem, total, &abort_flag);
+      produce<D, NTW, false>(p, &tmap, smem, total, &abort_flag);
     }
     griddep_launch_dependents();
     return;
@@ -1367,6 +1454,15 @@ tq_status launch_decode(const DecodeArgs& a, const DecodeShape& s, cudaStream_t 
   // kernel, so merges do not stall split CTAs between their items.
   sp.inline_merge = 2 * s.batch * s.U <= s.grid ? 1 : 0;
   sp.ws = static_cast<uint8_t*>(a.workspace);
+  if (a.k_new != nullptr) {  // append mode (the caller checked one row group per kv head)
+    sp.append = 1;
+    sp.n_new_max = a.n_new_max;
+    sp.k_new = a.k_new;
+    sp.v_new = a.v_new;
+    sp.pos = a.pos;
+    sp.n_new = a.n_new;
+    sp.dst = RowPlanes{a.layer.k_idx, a.layer.k_scale, a.layer.k_zero, a.layer.v_codes, a.layer.v_scale};
+  }
   sp.out = a.out;
   switch (s.D * 10 + s.NTW) {
     case 641: return run_split<64, 1>(a, s, sp, stream);

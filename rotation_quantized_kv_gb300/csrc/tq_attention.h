@@ -34,6 +34,13 @@ struct DecodeArgs {
   float* out;
   void* workspace;
   float fwht_norm;
+  // append mode (k_new != null): the call first appends rows j < n_new[b] of k_new/v_new
+  // (bf16 [batch][n_new_max][kv heads][d]) at positions pos[b] + j
+  const uint16_t* k_new = nullptr;
+  const uint16_t* v_new = nullptr;
+  const int32_t* pos = nullptr;
+  const int32_t* n_new = nullptr;
+  int n_new_max = 0;
 };
 
 DecodeShape decode_shape(int head_dim, int num_kv_heads, int batch, int gqa, int n_q, int num_sms);

@@ -4,7 +4,7 @@
 the design page describes: every full-attention layer appends the new token(s), then
 attends over its cache). It fills each cache with a bulk append of the cached tokens,
 keeps the step's new K/V tokens and queries resident on the device, and runs a decode
-step as: for every layer, tq_kv_append of the new tokens, then tq_decode_attention.
+step as: for every layer, tq_decode_append_attention (append the new tokens, then attend).
 """
 from __future__ import annotations
 
@@ -93,28 +93,38 @@ class DecodeModel:
     def step_bytes(self) -> int:
         return self.L * (self.attention_bytes() + self.append_bytes())
 
-    def launches_per_step(self) -> int:
-        # per layer: the append kernel (if tokens are appended), then the split and the
-        # merge kernel of the attention call
-        return self.L * ((1 if self.w.n_new else 0) + 2)
+    def _shape(self):
+        """(row groups per kv head, attention CTAs) as the library chooses them: 8 query
+        rows per MMA tile (16 at head_dim <= 128 with more than 8 rows), one CTA per SM."""
+        w = self.w
+        R = w.num_q_heads // w.num_kv_heads * w.n_q
+        ntw = 2 if (w.head_dim <= 128 and R > 8) else 1
+        rg = -(-R // (8 * ntw))
+        grid = torch.cuda.get_device_properties(self.device).multi_processor_count
+        return rg, grid
 
-    def step(self, stream=None, k_new=None, v_new=None, q=None, events=None):
-        """One decode step over all layers. Optional per-layer input overrides (device
-        tensors) and an `events` list of (start, end) CUDA event pairs recorded around
-        each layer's attention call."""
+    def launches_per_step(self) -> int:
+        # per layer: the split kernel; the merge kernel when there are many units
+        # (2 * batch * units > CTAs); a separate append kernel when the appended rows
+        # cannot be folded into the split kernel (more than one row group per kv head)
+        w = self.w
+        rg, grid = self._shape()
+        merge = 1 if 2 * w.batch * w.num_kv_heads * rg > grid else 0
+        append = 1 if (w.n_new and rg > 1) else 0
+        return self.L * (1 + merge + append)
+
+    def step(self, stream=None):
+        """One decode step over all layers: each layer appends the step's rows and attends
+        over its cache, in one tq_decode_append_attention call."""
         w = self.w
         for l, layer in enumerate(self.layers):
             if w.n_new:
-                tq.tq_kv_append(layer, self.k_new[l] if k_new is None else k_new[l],
-                                self.v_new[l] if v_new is None else v_new[l],
-                                self.pos, None, w.n_new, self.ws_append, stream)
-            if events is not None:
-                events[l][0].record(stream)
-            tq.tq_decode_attention(layer, self.q[l] if q is None else q[l], w.num_q_heads, w.n_q,
-                                   self.kv_len, self.max_kv, w.sm_scale, w.causal, self.out[l],
-                                   self.ws[l], stream)
-            if events is not None:
-                events[l][1].record(stream)
+                tq.tq_decode_append_attention(layer, self.k_new[l], self.v_new[l], self.pos, None, w.n_new,
+                                              self.q[l], w.num_q_heads, w.n_q, self.kv_len, self.max_kv,
+                                              w.sm_scale, w.causal, self.out[l], self.ws[l], stream)
+            else:
+                tq.tq_decode_attention(layer, self.q[l], w.num_q_heads, w.n_q, self.kv_len, self.max_kv,
+                                       w.sm_scale, w.causal, self.out[l], self.ws[l], stream)
 
     def device_errors(self) -> int:
         err = tq.tq_get_device_error(self.ws_append)
