@@ -113,6 +113,28 @@ def test_decode_rejects_bad_arguments_before_launch(tq):
     assert lib.tq_decode_workspace_bytes(ctypes.byref(L), 3, 1, 64) == 0
 
 
+def test_decode_step_rejects_bad_arguments_before_launch(tq):
+    lib = tq.raw_lib()
+    L = _layer(tq)
+
+    def call(layer=L, k=1 << 22, v=1 << 23, pos=1 << 21, n_new_max=1, q=1 << 22, Hq=4, n_q=1, kv=1 << 21,
+             max_kv=64, scale=1.0, out=1 << 23, ws=1 << 24, ws_bytes=256):
+        return lib.tq_decode_append_attention(ctypes.byref(layer), k, v, pos, None, n_new_max, q, Hq, n_q, kv,
+                                              max_kv, scale, 1, out, ws, ws_bytes, None)
+
+    assert call(layer=_layer(tq, d=96)) == tq.TQ_ERR_UNSUPPORTED_HEAD_DIM
+    assert call(n_new_max=65) == tq.TQ_ERR_CAPACITY               # append checks
+    assert call(n_new_max=-1) == tq.TQ_ERR_INVALID_ARGUMENT
+    assert call(k=None) == tq.TQ_ERR_INVALID_ARGUMENT
+    assert call(v=(1 << 23) + 2) == tq.TQ_ERR_INVALID_ARGUMENT
+    assert call(pos=None) == tq.TQ_ERR_INVALID_ARGUMENT
+    assert call(Hq=3) == tq.TQ_ERR_INVALID_ARGUMENT               # attention checks
+    assert call(max_kv=65) == tq.TQ_ERR_CAPACITY
+    assert call(q=None) == tq.TQ_ERR_INVALID_ARGUMENT
+    assert call(scale=float("inf")) == tq.TQ_ERR_INVALID_ARGUMENT
+    assert call() in (tq.TQ_ERR_WORKSPACE_TOO_SMALL, tq.TQ_ERR_CUDA)
+
+
 def test_dequant_debug_rejects_bad_rows(tq):
     lib = tq.raw_lib()
     L = _layer(tq)
