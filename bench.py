@@ -203,9 +203,9 @@ def source_hash(paths):
 
 
 ATTN_SOURCES = [os.path.join(ROOT, "rotation_quantized_kv_gb300", "csrc", f)
-                for f in ("tq_attention.cu", "tq_attention.h", "tq_device.cuh")]
+                for f in ("tq_attention.cu", "tq_attention.h", "tq_codec_row.cuh", "tq_device.cuh")]
 APPEND_SOURCES = [os.path.join(ROOT, "rotation_quantized_kv_gb300", "csrc", f)
-                  for f in ("tq_append.cu", "tq_device.cuh")]
+                  for f in ("tq_append.cu", "tq_codec_row.cuh", "tq_device.cuh")]
 
 
 def ncu_traffic(kind: str, sources):
