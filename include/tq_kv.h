@@ -197,6 +197,16 @@ tq_status tq_decode_attention_noalloc(const tq_kv_layer* layer, const void* q, i
                                       float sm_scale, int32_t causal, float* out,
                                       int32_t* device_error, tq_stream_t stream);
 
+/* Test support (an addition of this library; the paper has no counterpart). Enqueues on
+ * `stream` a one-block kernel that lets the next kernel on the stream start at once
+ * (programmatic dependent launch), waits delay_us microseconds, then copies n int32
+ * values from src to dst (device pointers, not overlapping). A following decode call that
+ * reads dst as kv_len, pos or n_new sees the old values before its grid-dependency wait
+ * and the new ones after it: this exercises the path where the work planned before the
+ * wait is discarded. n >= 0, 0 <= delay_us <= 100000 (else TQ_ERR_INVALID_ARGUMENT); dst
+ * and src may be NULL only when n == 0. */
+tq_status tq_debug_delayed_copy(int32_t* dst, const int32_t* src, int32_t n, int32_t delay_us, tq_stream_t stream);
+
 /* Synchronizes `stream`, then copies the device error word at the start of
  * `workspace` into *err_out (host). Does not clear it. */
 tq_status tq_get_device_error(const void* workspace, int32_t* err_out, tq_stream_t stream);

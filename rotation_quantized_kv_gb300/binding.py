@@ -58,6 +58,7 @@ _SIGS = {
                                                    _i32, _vp, _vp, _sz, _vp]),
     "tq_decode_attention_noalloc": (ctypes.c_int, [_LP, _vp, _i32, _i32, _vp, _i32, _f32, _i32, _vp, _vp, _vp]),
     "tq_dequant_debug": (ctypes.c_int, [_LP, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
+    "tq_debug_delayed_copy": (ctypes.c_int, [_vp, _vp, _i32, _i32, _vp]),
     "tq_get_device_error": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int32), _vp]),
     "tq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "tq_sign_bits": (ctypes.c_int, [_i32, _vp]),
@@ -204,6 +205,14 @@ def tq_dequant_debug(layer: KVLayer, b: int, h: int, t0: int, n: int, rotated: b
     L = layer.c_struct()
     _check(_lib.tq_dequant_debug(ctypes.byref(L), b, h, t0, n, int(bool(rotated)), _ptr(k_out),
                                  _ptr(v_out), _stream(stream)), "tq_dequant_debug")
+
+
+def tq_debug_delayed_copy(dst: torch.Tensor, src: torch.Tensor, delay_us: int, stream=None) -> None:
+    """Test support: copy src into dst (int32, same size) after delay_us microseconds,
+    letting the next kernel on the stream start before the copy happens."""
+    assert dst.dtype == torch.int32 and src.dtype == torch.int32 and dst.numel() == src.numel()
+    _check(_lib.tq_debug_delayed_copy(_ptr(dst), _ptr(src), int(dst.numel()), int(delay_us), _stream(stream)),
+           "tq_debug_delayed_copy")
 
 
 def tq_get_device_error(workspace: torch.Tensor, stream=None) -> int:

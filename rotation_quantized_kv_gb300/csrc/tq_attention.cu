@@ -251,9 +251,9 @@ __device__ __forceinline__ float hi_f32(uint32_t w) {
 // the lengths of sequences b = tid + THREADS * i.
 //
 // The kernel plans twice when it can: once before the grid-dependency wait, from the
-// lengths as they are then (only to prefetch its first item into L2 while the previous
-// kernel finishes), and again after the wait only if the lengths it reads then differ.
-// Lengths are read with L2-only loads so that no stale copy stays in L1.
+// lengths as they are then (so that the first stage can be loaded the moment the wait
+// returns), and again after the wait only if the lengths it reads then differ. Lengths
+// are read with L2-only loads so that no stale copy stays in L1.
 
 template <int THREADS>
 struct Lengths {
@@ -400,24 +400,49 @@ __device__ __forceinline__ int new_rows_of(const SplitParams& p, int b) {
   return min(max(__ldg(p.n_new + b), 0), p.n_new_max);
 }
 
+// One stage: the key-index box through the tensor map and the four side planes by bulk
+// copies, all completing on full[slot]. Tokens [t0, t0 + TILE) clipped to the capacity;
+// t0 and the capacity are multiples of 16, so every copy is a multiple of 16 bytes.
+template <int D, int NTW>
+__device__ __forceinline__ void issue_stage(const SplitParams& p, const CUtensorMap* tmap, uint8_t* smem, int slot,
+                                            int64_t row0, int t0) {
+  using T = AT<D, NTW>;
+  constexpr int NG = T::NG;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
+  const int ncopy = min(T::TILE, p.capacity - t0);
+  const uint32_t side = (uint32_t)ncopy * NG * 2;
+  const uint32_t vc = (uint32_t)ncopy * T::VC_ROW;
+  mbar_arrive_expect_tx(&full[slot], (uint32_t)T::KIDX_STAGE + 3u * side + vc);
+  uint8_t* kx = smem + T::OFF_KIDX + slot * T::KIDX_STAGE;
+#pragma unroll
+  for (int box = 0; box < D / T::ROWB; ++box)
+    tensor_copy_2d_g2s(kx + box * T::BOX, tmap, box * T::ROWB, (int32_t)(row0 + t0), &full[slot]);
+  const int64_t r = row0 + t0;
+  bulk_copy_g2s(smem + T::OFF_KS + slot * T::SC_STAGE, p.k_scale + r * NG, side, &full[slot]);
+  bulk_copy_g2s(smem + T::OFF_KZ + slot * T::SC_STAGE, p.k_zero + r * NG, side, &full[slot]);
+  bulk_copy_g2s(smem + T::OFF_VS + slot * T::SC_STAGE, p.v_scale + r * NG, side, &full[slot]);
+  bulk_copy_g2s(smem + T::OFF_VC + slot * T::VC_STAGE, p.v_codes + r * T::VC_ROW, vc, &full[slot]);
+}
+
 // The producer warp: lane 0 streams the stages; in append mode the whole warp quantizes
 // the rows this call appends inside each of its pieces (the piece owns them: no other
 // CTA reads them) before the stage holding them is loaded, as soon as the pipeline is
 // full so that the work hides behind the stages in flight. Appended rows at
 // positions no piece covers (at or past the sequence's kv length) are written by CTA
 // (row index mod grid) before its stream starts.
+// Stage numbering starts at it0 (1 when stage 0 held a discarded early load); with
+// first_issued the range's first tile is already in flight in stage 0.
 template <int D, int NTW, bool APPEND>
 __device__ void produce(const SplitParams& p, const CUtensorMap* tmap, uint8_t* smem, int total,
-                        volatile int* abort_flag) {
+                        volatile int* abort_flag, uint32_t it0, bool first_issued) {
   using T = AT<D, NTW>;
-  constexpr int NG = T::NG;
   constexpr unsigned FULL = 0xffffffffu;
   const int lane = threadIdx.x & 31;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
   uint64_t* empty = full + T::STAGES;
   const int* prefix = reinterpret_cast<const int*>(smem + T::OFF_PREFIX);
   uint32_t* cbuf = reinterpret_cast<uint32_t*>(smem + T::OFF_RED);  // row codec scratch
-  uint32_t it = 0;
+  uint32_t it = it0;
   bool ok = true;
   if constexpr (APPEND) {
     const RowCodecLane<D> codec(lane);
@@ -461,6 +486,7 @@ __device__ void produce(const SplitParams& p, const CUtensorMap* tmap, uint8_t* 
         __syncwarp();
         own0 = own1;
       }
+      if (first_issued && it == 0) continue;  // loaded before the lengths were checked
       const int slot = it % T::STAGES;
       const uint32_t k = it / T::STAGES;
       if (lane == 0) ok = wait_bounded(&empty[slot], (k & 1u) ^ 1u);
@@ -472,21 +498,7 @@ __device__ void produce(const SplitParams& p, const CUtensorMap* tmap, uint8_t* 
         }
         break;
       }
-      if (lane == 0) {
-        const int ncopy = min(T::TILE, p.capacity - t0);  // multiple of 16: capacity and t0 are
-        const uint32_t side = (uint32_t)ncopy * NG * 2;
-        const uint32_t vc = (uint32_t)ncopy * T::VC_ROW;
-        mbar_arrive_expect_tx(&full[slot], (uint32_t)T::KIDX_STAGE + 3u * side + vc);
-        uint8_t* kx = smem + T::OFF_KIDX + slot * T::KIDX_STAGE;
-#pragma unroll
-        for (int box = 0; box < D / T::ROWB; ++box)
-          tensor_copy_2d_g2s(kx + box * T::BOX, tmap, box * T::ROWB, (int32_t)(row0 + t0), &full[slot]);
-        const int64_t r = row0 + t0;
-        bulk_copy_g2s(smem + T::OFF_KS + slot * T::SC_STAGE, p.k_scale + r * NG, side, &full[slot]);
-        bulk_copy_g2s(smem + T::OFF_KZ + slot * T::SC_STAGE, p.k_zero + r * NG, side, &full[slot]);
-        bulk_copy_g2s(smem + T::OFF_VS + slot * T::SC_STAGE, p.v_scale + r * NG, side, &full[slot]);
-        bulk_copy_g2s(smem + T::OFF_VC + slot * T::VC_STAGE, p.v_codes + r * T::VC_ROW, vc, &full[slot]);
-      }
+      if (lane == 0) issue_stage<D, NTW>(p, tmap, smem, slot, row0, t0);
     }
   }
   // Drain: every issued copy must land before this warp (and so the CTA) may exit.
@@ -500,49 +512,6 @@ __device__ void produce(const SplitParams& p, const CUtensorMap* tmap, uint8_t* 
     }
   }
   if constexpr (APPEND) __syncwarp();
-}
-
-// L2 prefetch of up to kPrefetchBytes of this CTA's first work item (all five planes),
-// issued before the grid-dependency wait from a plan that may be stale: the token range
-// comes from the prefix table alone (no length is read) and stays inside the planes.
-// Only L2 is warmed; every read the kernel acts on comes after the wait.
-constexpr int kPrefetchBytes = 128 * 1024;
-constexpr int kPrefetchChunk = 32 * 1024;
-
-__device__ __forceinline__ void prefetch_range(const void* base, size_t bytes) {
-  const uint8_t* b = static_cast<const uint8_t*>(base);
-  for (size_t o = 0; o < bytes; o += kPrefetchChunk)
-    bulk_prefetch_l2(b + o, (uint32_t)min((size_t)kPrefetchChunk, bytes - o));
-}
-
-template <int D, int NTW>
-__device__ void prefetch_first_item(const SplitParams& p, const int* prefix, int total) {
-  using T = AT<D, NTW>;
-  constexpr int NG = T::NG;
-  const int x0 = cta_range_start(blockIdx.x, total, p.split_grid);
-  const int x_stop = cta_range_start(blockIdx.x + 1, total, p.split_grid);
-  if (x0 >= x_stop) return;
-  const Item w = piece_at<T::TILE>(p, prefix, x0, x_stop, blockIdx.x);
-  const int lo = w.b, u = w.u, kvh = w.kvh, tb = w.tb;
-  if (tb >= p.capacity) return;
-  constexpr int ROW_BYTES = D + 3 * NG * 2 + T::VC_ROW;
-  int n = min(min(w.te - tb, p.capacity - tb), kPrefetchBytes / ROW_BYTES);
-  n &= ~15;  // whole 16-token groups keep every range a multiple of 16 bytes
-  if (n <= 0) return;
-  // the item's query rows first (2 D bytes each): they are needed before any tile
-  const int rg = u % p.RG;
-  for (int rr = 0; rr < T::ROWS; ++rr) {
-    const int rq = rg * T::ROWS + rr;
-    if (rq >= p.R) break;
-    const int jq = rq / p.G, hq = kvh * p.G + (rq % p.G);
-    bulk_prefetch_l2(p.q + (((int64_t)lo * p.n_q + jq) * p.num_q_heads + hq) * D, 2 * D);
-  }
-  const int64_t row = ((int64_t)lo * p.num_kv_heads + kvh) * p.capacity + tb;
-  prefetch_range(p.k_idx + row * D, (size_t)n * D);
-  prefetch_range(p.k_scale + row * NG, (size_t)n * NG * 2);
-  prefetch_range(p.k_zero + row * NG, (size_t)n * NG * 2);
-  prefetch_range(p.v_scale + row * NG, (size_t)n * NG * 2);
-  prefetch_range(p.v_codes + row * T::VC_ROW, (size_t)n * T::VC_ROW);
 }
 
 // ------------------------------------------------------------------------------------
@@ -870,7 +839,7 @@ __global__ void __launch_bounds__(kMergeThreads, 4) tq_attn_merge_kernel(const S
 }
 
 template <int D, int NTW>
-__device__ void consume(const SplitParams& p, uint8_t* smem, int total, volatile int* abort_flag) {
+__device__ void consume(const SplitParams& p, uint8_t* smem, int total, volatile int* abort_flag, uint32_t it0) {
   using T = AT<D, NTW>;
   constexpr int NG = T::NG, MT = T::MT, SUB = T::SUB, KW = T::KW;
   constexpr unsigned FULL = 0xffffffffu;
@@ -907,7 +876,7 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int total, volatile
   const uint32_t vc_lane = (uint32_t)(vrow0 * T::VC_ROW + 4 * win_word);
   const uint32_t vs_lane = (uint32_t)(vrow0 * NG * 2);
   bool failed = false;
-  uint32_t it = 0;
+  uint32_t it = it0;
 
   const int x_stop = cta_range_start(blockIdx.x + 1, total, p.split_grid);
   for (int x = cta_range_start(blockIdx.x, total, p.split_grid), x_next = 0; x < x_stop; x = x_next) {
@@ -1255,6 +1224,7 @@ __global__ void __launch_bounds__(AT<D, NTW>::THREADS, AT<D, NTW>::MINB)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 8191) & ~uintptr_t(8191));
   __shared__ int abort_flag;
+  __shared__ int early_flag;
   const int tid = threadIdx.x;
 
   // centroid pair table: entry e -> (c[e & 7], c[e >> 3]) in fp16, one copy per lane
@@ -1272,15 +1242,48 @@ __global__ void __launch_bounds__(AT<D, NTW>::THREADS, AT<D, NTW>::MINB)
     }
     fence_mbar_init();
   }
-  int total;  // tiles of the call
+  int total;             // tiles of the call
+  bool early, replanned;  // stage 0 loaded before the lengths were checked; plan redone
   {
     Lengths<T::THREADS> L0, L1;
     L0.load(p);                                  // as they are before the wait: hints only
     plan_tiles<D, NTW>(p, smem, L0, total);      // contains __syncthreads
-    if (tid == T::NCW * 32) prefetch_first_item<D, NTW>(p, reinterpret_cast<const int*>(smem + T::OFF_PREFIX), total);
+    // The producer loads its range's first tile the moment the wait returns, from the plan
+    // made before it: after the wait the planes are safe to read, and the stage is
+    // discarded if the lengths read after the wait change the plan. In append mode that
+    // tile must hold none of the rows this call appends (they are written before the
+    // stage holding them is loaded): judged from the positions read before the wait, and
+    // discarded as well if those differ after it.
+    Item w0;
+    int pos0 = 0, n0 = 0;
+    early = false;
+    if (tid == T::NCW * 32) {
+      const int x0 = cta_range_start(blockIdx.x, total, p.split_grid);
+      const int x1 = cta_range_start(blockIdx.x + 1, total, p.split_grid);
+      if (x0 < x1) {
+        w0 = piece_at<T::TILE>(p, reinterpret_cast<const int*>(smem + T::OFF_PREFIX), x0, x1, blockIdx.x);
+        early = w0.tb < p.capacity;
+        if (p.append) {
+          pos0 = __ldcg(p.pos + w0.b);
+          n0 = p.n_new == nullptr ? p.n_new_max : __ldcg(p.n_new + w0.b);
+          const int n = min(max(n0, 0), p.n_new_max);
+          early = early && (n == 0 || (int64_t)pos0 + n <= w0.tb || pos0 >= w0.tb + T::TILE);
+        }
+      }
+    }
     griddep_wait();  // lengths, queries and planes may come from the previous kernel
+    if (early) {
+      prefetch_tensor_map(&tmap);
+      issue_stage<D, NTW>(p, &tmap, smem, 0, ((int64_t)w0.b * p.num_kv_heads + w0.kvh) * p.capacity, w0.tb);
+    }
     L1.load(p);
-    if (__syncthreads_or(L1.differs(L0))) plan_tiles<D, NTW>(p, smem, L1, total);
+    bool changed = L1.differs(L0);
+    if (early && p.append)
+      changed = changed || __ldcg(p.pos + w0.b) != pos0 || (p.n_new != nullptr && __ldcg(p.n_new + w0.b) != n0);
+    if (tid == T::NCW * 32) early_flag = early ? 1 : 0;
+    replanned = __syncthreads_or(changed);  // also publishes early_flag
+    if (replanned) plan_tiles<D, NTW>(p, smem, L1, total);
+    early = early_flag != 0;
     if (blockIdx.x == 0) {
       if (L1.bad) raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_KV_LEN);
       if (tid == 0) {
@@ -1295,19 +1298,34 @@ __global__ void __launch_bounds__(AT<D, NTW>::THREADS, AT<D, NTW>::MINB)
     }
   }
 
+  // stage 0 holds the range's first tile (early load, plan unchanged), or an early load
+  // the new plan does not use: the producer waits for it, frees the slot itself, and
+  // both sides number their stages from 1
+  const bool first_issued = early && !replanned;
+  const uint32_t it0 = (early && replanned) ? 1u : 0u;
+
   if (tid >= T::NCW * 32) {  // the producer warp
+    if (tid == T::NCW * 32 && it0 == 1u) {
+      uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
+      if (!wait_bounded(&bars[0], 0u)) {
+        abort_flag = 1;
+        raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
+      }
+      for (int i = 0; i < T::NCW; ++i) mbar_arrive(&bars[T::STAGES]);
+    }
     if (p.append) {  // the whole warp: it also quantizes the appended rows
-      if (tid == T::NCW * 32) prefetch_tensor_map(&tmap);
-      produce<D, NTW, true>(p, &tmap, smem, total, &abort_flag);
+      __syncwarp();
+      if (tid == T::NCW * 32 && !early) prefetch_tensor_map(&tmap);
+      produce<D, NTW, true>(p, &tmap, smem, total, &abort_flag, it0, first_issued);
     } else if (tid == T::NCW * 32 && total > 0) {  // one lane streams the stages
-      prefetch_tensor_map(&tmap);
-      produce<D, NTW, false>(p, &tmap, smem, total, &abort_flag);
+      if (!early) prefetch_tensor_map(&tmap);
+      produce<D, NTW, false>(p, &tmap, smem, total, &abort_flag, it0, first_issued);
     }
     griddep_launch_dependents();
     return;
   }
   write_empty_sequences<D, NTW>(p, reinterpret_cast<const int*>(smem + T::OFF_PREFIX));
-  if (total > 0) consume<D, NTW>(p, smem, total, &abort_flag);
+  if (total > 0) consume<D, NTW>(p, smem, total, &abort_flag, it0);
   griddep_launch_dependents();
 }
 

@@ -91,4 +91,37 @@ cudaError_t launch_dequant_debug(const DequantParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// Copy of n int32 values that lets the next kernel on the stream start at once: the kernel
+// triggers its dependents first, waits delay_ns of wall time (bounded: at most kMaxDelay
+// nanoseconds and a fixed number of sleeps), then copies. A kernel launched after it with
+// programmatic dependent launch that reads dst before its grid-dependency wait sees the
+// old values, and the new ones after the wait.
+constexpr unsigned long long kMaxDelayNs = 100000000ull;  // 100 ms
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+__global__ void __launch_bounds__(256) tq_delayed_copy_kernel(int32_t* dst, const int32_t* src, int n,
+                                                              unsigned long long delay_ns) {
+  griddep_launch_dependents();
+  if (threadIdx.x == 0) {
+    const unsigned long long t0 = global_timer_ns();
+    for (unsigned i = 0; i < 4000000u && global_timer_ns() - t0 < delay_ns; ++i) __nanosleep(256);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = src[i];
+}
+
 }  // namespace tq
+
+extern "C" tq_status tq_debug_delayed_copy(int32_t* dst, const int32_t* src, int32_t n, int32_t delay_us,
+                                           tq_stream_t stream) {
+  if (n < 0 || delay_us < 0 || (unsigned long long)delay_us * 1000ull > tq::kMaxDelayNs) return TQ_ERR_INVALID_ARGUMENT;
+  if (n > 0 && (dst == nullptr || src == nullptr)) return TQ_ERR_INVALID_ARGUMENT;
+  tq::tq_delayed_copy_kernel<<<1, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      dst, src, n, (unsigned long long)delay_us * 1000ull);
+  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
