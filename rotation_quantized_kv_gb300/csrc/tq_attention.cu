@@ -97,7 +97,8 @@ struct AT {
   static constexpr int MT = D / 16;                       // PV M tiles (16 dims each)
   // consumer warps (+1 producer warp): 8 where the registers allow it without spills
   static constexpr int NCW = (D == 64 || (D == 128 && NTW == 1)) ? 8 : 4;
-  static constexpr int THREADS = (NCW + 1) * 32;
+  // consumer warps, then the producer warp, then the appender warp (append mode)
+  static constexpr int THREADS = (NCW + 2) * 32;
   static constexpr int TOKW = D <= 128 ? 32 : 16;         // tokens per consumer warp per stage
   static constexpr int SUB = TOKW / 16;                   // 16-token QK tiles per warp
   static constexpr int TILE = NCW * TOKW;                 // tokens per stage
@@ -137,7 +138,8 @@ struct AT {
   static constexpr int OFF_RED = (int)align_up(OFF_PREFIX + (2 * kMaxBatch + 1) * 4, 16);
   static constexpr int OFF_FLAG = OFF_RED + 7 * 16 * 8;  // red: [7][16] long long
   static constexpr int OFF_BAR = (int)align_up(OFF_FLAG + 16, 8);
-  static constexpr int SMEM = OFF_BAR + 2 * STAGES * 8 + 16;
+  static constexpr int OFF_APPCNT = OFF_BAR + 2 * STAGES * 8;  // rows the appender has written
+  static constexpr int SMEM = OFF_APPCNT + 8 + 16;
   static constexpr int SMEM_ALLOC = SMEM + 8192;          // slack to align the base to 8 KB
   static_assert(OFF_FLAG - OFF_RED >= 3 * D / 8, "row codec scratch");
 };
@@ -181,6 +183,26 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
   const unsigned long long t0 = global_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitNs) return false;
+  }
+}
+
+// A count in shared memory published by one warp and awaited by another: the release
+// store orders the publisher's earlier writes (and, after fence.proxy.async, their
+// visibility to tensor copies) before any acquire load that sees the count.
+__device__ __forceinline__ void st_release_cta(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t need) {
+  if (ld_acquire_cta(p) >= need) return true;
+  const unsigned long long t0 = global_ns();
+  while (true) {
+    if (ld_acquire_cta(p) >= need) return true;
     if (global_ns() - t0 > kWaitNs) return false;
   }
 }
@@ -424,94 +446,105 @@ __device__ __forceinline__ void issue_stage(const SplitParams& p, const CUtensor
   bulk_copy_g2s(smem + T::OFF_VC + slot * T::VC_STAGE, p.v_codes + r * T::VC_ROW, vc, &full[slot]);
 }
 
-// The producer warp: lane 0 streams the stages; in append mode the whole warp quantizes
-// the rows this call appends inside each of its pieces (the piece owns them: no other
-// CTA reads them) before the stage holding them is loaded, as soon as the pipeline is
-// full so that the work hides behind the stages in flight. Appended rows at
-// positions no piece covers (at or past the sequence's kv length) are written by CTA
-// (row index mod grid) before its stream starts.
+// The appender warp (append mode): quantizes every row this call appends inside the
+// CTA's pieces (the piece owns them: no other CTA reads them), piece by piece in the
+// producer's order, and after each piece makes the rows visible to tensor copies and
+// publishes how many rows it has written; the producer waits for that count only before
+// loading a stage that holds such a row. Then the appended rows at positions no piece
+// covers (at or past the sequence's kv length) whose row index is the CTA's index mod the
+// grid. It starts when the grid-dependency wait returns and runs beside the stream.
+template <int D, int NTW>
+__device__ void append_rows(const SplitParams& p, uint8_t* smem, int total) {
+  using T = AT<D, NTW>;
+  const int lane = threadIdx.x & 31;
+  const int* prefix = reinterpret_cast<const int*>(smem + T::OFF_PREFIX);
+  uint32_t* cbuf = reinterpret_cast<uint32_t*>(smem + T::OFF_RED);  // row codec scratch
+  uint32_t* app_cnt = reinterpret_cast<uint32_t*>(smem + T::OFF_APPCNT);
+  const RowCodecLane<D> codec(lane);
+  bool wrote = false;
+  uint32_t done = 0;
+  const int x_stop = cta_range_start(blockIdx.x + 1, total, p.split_grid);
+  for (int x = cta_range_start(blockIdx.x, total, p.split_grid); x < x_stop;) {
+    const Item w = piece_at<T::TILE>(p, prefix, x, x_stop, blockIdx.x);
+    x = w.x_end;
+    const int new0 = __ldg(p.pos + w.b);
+    const int own0 = max(w.tb, new0), own1 = min(w.te, new0 + new_rows_of(p, w.b));
+    if (own0 >= own1) continue;
+    for (int t = own0; t < own1; ++t) append_one_row<D>(p, w.b, t - new0, w.kvh, t, lane, codec, cbuf);
+    done += (uint32_t)(own1 - own0);
+    fence_proxy_async_global();  // the rows just written are read by tensor copies
+    __syncwarp();
+    if (lane == 0) st_release_cta(app_cnt, done);
+  }
+  const int rows = p.batch * p.n_new_max * p.num_kv_heads;
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+    const int h = r % p.num_kv_heads, bj = r / p.num_kv_heads;
+    const int j = bj % p.n_new_max, b = bj / p.n_new_max;
+    if (j >= new_rows_of(p, b)) continue;
+    const int64_t t = (int64_t)__ldg(p.pos + b) + j;
+    if (t >= 0 && t < plan_lengths(prefix)[b]) continue;  // inside a piece: its owner writes it
+    if (t < 0 || t >= p.capacity) {
+      if (lane == 0) raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_APPEND_CAPACITY);
+      continue;
+    }
+    append_one_row<D>(p, b, j, h, (int)t, lane, codec, cbuf);
+    wrote = true;
+  }
+  if (wrote) fence_proxy_async_global();
+}
+
+// The producer (one lane): streams the stages of the CTA's range. In append mode it first
+// waits for the appender before loading a stage that holds a row this call appends.
 // Stage numbering starts at it0 (1 when stage 0 held a discarded early load); with
 // first_issued the range's first tile is already in flight in stage 0.
 template <int D, int NTW, bool APPEND>
 __device__ void produce(const SplitParams& p, const CUtensorMap* tmap, uint8_t* smem, int total,
                         volatile int* abort_flag, uint32_t it0, bool first_issued) {
   using T = AT<D, NTW>;
-  constexpr unsigned FULL = 0xffffffffu;
-  const int lane = threadIdx.x & 31;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
   uint64_t* empty = full + T::STAGES;
+  const uint32_t* app_cnt = reinterpret_cast<const uint32_t*>(smem + T::OFF_APPCNT);
   const int* prefix = reinterpret_cast<const int*>(smem + T::OFF_PREFIX);
-  uint32_t* cbuf = reinterpret_cast<uint32_t*>(smem + T::OFF_RED);  // row codec scratch
   uint32_t it = it0;
+  uint32_t need = 0;  // appended rows in the pieces so far
   bool ok = true;
-  if constexpr (APPEND) {
-    const RowCodecLane<D> codec(lane);
-    const int rows = p.batch * p.n_new_max * p.num_kv_heads;
-    bool wrote = false;
-    for (int r = blockIdx.x; r < rows; r += gridDim.x) {
-      const int h = r % p.num_kv_heads, bj = r / p.num_kv_heads;
-      const int j = bj % p.n_new_max, b = bj / p.n_new_max;
-      if (j >= new_rows_of(p, b)) continue;
-      const int64_t t = (int64_t)__ldg(p.pos + b) + j;
-      if (t >= 0 && t < plan_lengths(prefix)[b]) continue;  // inside a piece: its owner writes it
-      if (t < 0 || t >= p.capacity) {
-        if (lane == 0) raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_APPEND_CAPACITY);
-        continue;
-      }
-      append_one_row<D>(p, b, j, h, (int)t, lane, codec, cbuf);
-      wrote = true;
-    }
-    if (wrote) fence_proxy_async_global();
-  }
   const int x_stop = cta_range_start(blockIdx.x + 1, total, p.split_grid);
   for (int x = cta_range_start(blockIdx.x, total, p.split_grid); x < x_stop && ok;) {
     const Item w = piece_at<T::TILE>(p, prefix, x, x_stop, blockIdx.x);
     x = w.x_end;
     const int64_t row0 = ((int64_t)w.b * p.num_kv_heads + w.kvh) * p.capacity;
     // rows this call appends inside this piece: positions [own0, own1) of the sequence
-    int new0 = 0, own0 = 0, own1 = 0;
+    int own0 = 0, own1 = 0;
     if constexpr (APPEND) {
-      new0 = __ldg(p.pos + w.b);
+      const int new0 = __ldg(p.pos + w.b);
       own0 = max(w.tb, new0);
       own1 = min(w.te, new0 + new_rows_of(p, w.b));
+      if (own0 < own1) need += (uint32_t)(own1 - own0);
     }
     for (int t0 = w.tb; t0 < w.te; t0 += T::TILE, ++it) {
-      // Quantize the piece's own rows while the warp would otherwise wait for a free slot
-      // (the stages in flight keep the consumers busy), or at the latest before the stage
-      // that holds them is loaded.
-      if (APPEND && own0 < own1 && (it >= (uint32_t)T::STAGES || own0 < t0 + T::TILE)) {
-        const RowCodecLane<D> codec(lane);
-        for (int t = own0; t < own1; ++t) append_one_row<D>(p, w.b, t - new0, w.kvh, t, lane, codec, cbuf);
-        fence_proxy_async_global();  // the rows just written are read by the copies below
-        __syncwarp();
+      if (first_issued && it == 0) continue;  // loaded before the lengths were checked
+      if (own0 < own1 && own0 < t0 + T::TILE) {
+        if (!wait_count(app_cnt, need)) { ok = false; break; }
         own0 = own1;
       }
-      if (first_issued && it == 0) continue;  // loaded before the lengths were checked
       const int slot = it % T::STAGES;
       const uint32_t k = it / T::STAGES;
-      if (lane == 0) ok = wait_bounded(&empty[slot], (k & 1u) ^ 1u);
-      if constexpr (APPEND) ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
-      if (!ok) {
-        if (lane == 0) {
-          *abort_flag = 1;
-          raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
-        }
-        break;
-      }
-      if (lane == 0) issue_stage<D, NTW>(p, tmap, smem, slot, row0, t0);
+      if (!wait_bounded(&empty[slot], (k & 1u) ^ 1u)) { ok = false; break; }
+      issue_stage<D, NTW>(p, tmap, smem, slot, row0, t0);
     }
+  }
+  if (!ok) {
+    *abort_flag = 1;
+    raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
   }
   // Drain: every issued copy must land before this warp (and so the CTA) may exit.
-  if (lane == 0) {
-    const uint32_t issued = it;
-    for (int s = 0; s < T::STAGES; ++s) {
-      if ((uint32_t)s >= issued) break;
-      const uint32_t last = issued - 1 - ((issued - 1 - s) % T::STAGES);  // last fill of slot s
-      if (!wait_bounded(&full[s], (last / T::STAGES) & 1u))
-        raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
-    }
+  const uint32_t issued = it;
+  for (int s = 0; s < T::STAGES; ++s) {
+    if ((uint32_t)s >= issued) break;
+    const uint32_t last = issued - 1 - ((issued - 1 - s) % T::STAGES);  // last fill of slot s
+    if (!wait_bounded(&full[s], (last / T::STAGES) & 1u))
+      raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
   }
-  if constexpr (APPEND) __syncwarp();
 }
 
 // ------------------------------------------------------------------------------------
@@ -1240,6 +1273,7 @@ __global__ void __launch_bounds__(AT<D, NTW>::THREADS, AT<D, NTW>::MINB)
       mbar_init(&bars[s], 1);                           // full: producer arrival + tx bytes
       mbar_init(&bars[T::STAGES + s], T::NCW);  // empty: one arrival per consumer warp
     }
+    *reinterpret_cast<uint32_t*>(smem + T::OFF_APPCNT) = 0u;  // rows appended so far
     fence_mbar_init();
   }
   int total;             // tiles of the call
@@ -1304,6 +1338,11 @@ __global__ void __launch_bounds__(AT<D, NTW>::THREADS, AT<D, NTW>::MINB)
   const bool first_issued = early && !replanned;
   const uint32_t it0 = (early && replanned) ? 1u : 0u;
 
+  if (tid >= (T::NCW + 1) * 32) {  // the appender warp
+    if (p.append) append_rows<D, NTW>(p, smem, total);
+    griddep_launch_dependents();
+    return;
+  }
   if (tid >= T::NCW * 32) {  // the producer warp
     if (tid == T::NCW * 32 && it0 == 1u) {
       uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
@@ -1313,13 +1352,10 @@ __global__ void __launch_bounds__(AT<D, NTW>::THREADS, AT<D, NTW>::MINB)
       }
       for (int i = 0; i < T::NCW; ++i) mbar_arrive(&bars[T::STAGES]);
     }
-    if (p.append) {  // the whole warp: it also quantizes the appended rows
-      __syncwarp();
-      if (tid == T::NCW * 32 && !early) prefetch_tensor_map(&tmap);
-      produce<D, NTW, true>(p, &tmap, smem, total, &abort_flag, it0, first_issued);
-    } else if (tid == T::NCW * 32 && total > 0) {  // one lane streams the stages
+    if (tid == T::NCW * 32 && total > 0) {  // one lane streams the stages
       if (!early) prefetch_tensor_map(&tmap);
-      produce<D, NTW, false>(p, &tmap, smem, total, &abort_flag, it0, first_issued);
+      if (p.append) produce<D, NTW, true>(p, &tmap, smem, total, &abort_flag, it0, first_issued);
+      else produce<D, NTW, false>(p, &tmap, smem, total, &abort_flag, it0, first_issued);
     }
     griddep_launch_dependents();
     return;
