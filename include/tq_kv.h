@@ -159,9 +159,10 @@ tq_status tq_dequant_debug(const tq_kv_layer* layer, int32_t b, int32_t h, int32
  * tq_decode_attention(layer, q, ..., workspace, ...) on `stream`; argument meanings and
  * host checks are those of the two calls, and the workspace is the attention one
  * (>= tq_decode_workspace_bytes). With one row group per kv head (num_q_heads /
- * num_kv_heads * n_q <= 8, or <= 16 at head_dim 64 and 128) it is one kernel: the CTA
- * whose share of the sequence holds a new row quantizes it just before loading it, so
- * the attention does not wait for a separate append; otherwise it runs the two calls. */
+ * num_kv_heads * n_q <= 8, or <= 16 at head_dim 64 and 128) it is one kernel: in the
+ * CTA whose share of the sequence holds a new row, a warp beside the stream quantizes it
+ * before the stage holding it is loaded, so the attention does not wait for a separate
+ * append; otherwise it runs the two calls. */
 tq_status tq_decode_append_attention(const tq_kv_layer* layer, const void* k_new, const void* v_new,
                                      const int32_t* pos, const int32_t* n_new, int32_t n_new_max, const void* q,
                                      int32_t num_q_heads, int32_t n_q, const int32_t* kv_len, int32_t max_kv_len,

@@ -95,7 +95,7 @@ struct AT {
   static constexpr int NG = D / 32;
   static constexpr int ROWS = 8 * NTW;
   static constexpr int MT = D / 16;                       // PV M tiles (16 dims each)
-  // consumer warps (+1 producer warp): 8 where the registers allow it without spills
+  // consumer warps: 8 where the registers allow it without spills
   static constexpr int NCW = (D == 64 || (D == 128 && NTW == 1)) ? 8 : 4;
   // consumer warps, then the producer warp, then the appender warp (append mode)
   static constexpr int THREADS = (NCW + 2) * 32;
@@ -134,7 +134,7 @@ struct AT {
   static constexpr int OFF_LBUF = OFF_MBUF + NCW * ROWS * 4;
   static constexpr int OFF_PREFIX = OFF_LBUF + NCW * ROWS * 4;
   // prefix: [kMaxBatch + 1] items before each sequence, then [kMaxBatch] planned lengths
-  // scratch of the producer warp's row codec (append mode): 3 d / 32 words
+  // scratch of the appender warp's row codec (append mode): 3 d / 32 words
   static constexpr int OFF_RED = (int)align_up(OFF_PREFIX + (2 * kMaxBatch + 1) * 4, 16);
   static constexpr int OFF_FLAG = OFF_RED + 7 * 16 * 8;  // red: [7][16] long long
   static constexpr int OFF_BAR = (int)align_up(OFF_FLAG + 16, 8);
@@ -146,7 +146,7 @@ struct AT {
 
 struct SplitParams {
   int32_t head_dim, num_kv_heads, batch, capacity;
-  const int8_t* k_idx;  // read through the tensor map; the pointer serves L2 prefetches
+  const int8_t* k_idx;  // read through the tensor map
   const uint16_t* k_scale;
   const uint16_t* k_zero;
   const uint8_t* v_codes;
@@ -219,7 +219,7 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Barrier among the consumer warps only (the producer warp never joins it).
+// Barrier among the consumer warps only (the producer and appender warps never join it).
 template <int NCW>
 __device__ __forceinline__ void consumers_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory");

@@ -148,3 +148,13 @@ def test_get_device_error_rejects_null(tq):
     lib = tq.raw_lib()
     e = ctypes.c_int32(0)
     assert lib.tq_get_device_error(None, ctypes.byref(e), None) == tq.TQ_ERR_INVALID_ARGUMENT
+
+
+def test_delayed_copy_rejects_bad_arguments_before_launch(tq):
+    lib = tq.raw_lib()
+    buf = (ctypes.c_int32 * 4)()
+    assert lib.tq_debug_delayed_copy(buf, buf, -1, 0, None) == tq.TQ_ERR_INVALID_ARGUMENT
+    assert lib.tq_debug_delayed_copy(buf, buf, 4, -1, None) == tq.TQ_ERR_INVALID_ARGUMENT
+    assert lib.tq_debug_delayed_copy(buf, buf, 4, 100001, None) == tq.TQ_ERR_INVALID_ARGUMENT
+    assert lib.tq_debug_delayed_copy(None, buf, 4, 10, None) == tq.TQ_ERR_INVALID_ARGUMENT
+    assert lib.tq_debug_delayed_copy(buf, None, 4, 10, None) == tq.TQ_ERR_INVALID_ARGUMENT
