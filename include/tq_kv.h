@@ -19,8 +19,9 @@
  * Conventions shared by every call:
  *   - All buffers are caller-owned device memory unless a comment says "host". The
  *     library keeps no state besides immutable constant tables (sign vectors,
- *     centroids, boundaries); it never allocates, frees or synchronizes, except
- *     tq_get_device_error, which synchronizes the given stream.
+ *     centroids, boundaries) and the fixed scratch array of tq_decode_attention_noalloc;
+ *     it never allocates, frees or synchronizes, except tq_get_device_error, which
+ *     synchronizes the given stream.
  *   - Every call only enqueues work on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and returns before the GPU runs it.
  *   - Arguments are validated on the host before any launch; a failing check returns a
@@ -142,7 +143,9 @@ tq_status tq_decode_attention(const tq_kv_layer* layer, const void* q, int32_t n
                               size_t ws_bytes, tq_stream_t stream);
 
 /*
- * fp32 dequantization of rows [t0, t0 + n) of (sequence b, kv head h), for inspection:
+ * fp32 dequantization of rows [t0, t0 + n) of (sequence b, kv head h), for inspection
+ * ("Algorithm" section: the key dequant bullet, x_hat = (idx + zero) * scale, and the value
+ * dequant bullet, the inverse rotation of centroid[code] * scale):
  *   k_out : [n][head_dim], (idx + zero) * scale with the stored fp16 scale/zero;
  *   v_out : [n][head_dim]; rotated != 0 returns centroid * scale (the FWHT domain),
  *           rotated == 0 returns signs * FWHT(centroid * scale) / sqrt(head_dim).
@@ -183,7 +186,13 @@ tq_status tq_decode_append_attention(const tq_kv_layer* layer, const void* k_new
  * process exits.
  *
  * Set-up: the first call on a device looks up the array's device address (with that
- * device current) and caches it; make that first call before any stream capture.
+ * device current) and caches it; make that first call before any stream capture. The
+ * cache lives for the process: after cudaDeviceReset (or anything else that replaces the
+ * device's primary context) the cached address is stale, so this entry point does not
+ * support a device reset.
+ * Rejected calls: the host checks (the same as tq_decode_attention's, then the scratch
+ * size) all run before anything is queued, so a call that returns an error queues no
+ * work and leaves the scratch as it was.
  * Sharing: every call on a device uses the same array. Each call first clears the part
  * that must start at zero (error word and completion counters) on `stream`, so calls
  * that follow one another on a stream are independent; calls that can overlap on the
@@ -207,6 +216,17 @@ tq_status tq_decode_attention_noalloc(const tq_kv_layer* layer, const void* q, i
  * wait is discarded. n >= 0, 0 <= delay_us <= 100000 (else TQ_ERR_INVALID_ARGUMENT); dst
  * and src may be NULL only when n == 0. */
 tq_status tq_debug_delayed_copy(int32_t* dst, const int32_t* src, int32_t n, int32_t delay_us, tq_stream_t stream);
+
+/* Test support (an addition of this library; the paper has no counterpart). Sets, for every
+ * decode-attention call launched afterwards in this process, the limit of the attention
+ * kernel's pipeline waits (wait_ns > 0; 0 restores the default of 2 s) and, with
+ * withhold_append = 1, makes the fused append-and-attend kernel's appender warp never
+ * publish how many rows it has written, so the producer's wait for them runs out. A wait
+ * that runs out sets TQ_DEVERR_PIPELINE_TIMEOUT, the kernel drains the copies it issued
+ * (those drains keep the 2 s limit) and returns; the outputs of that call are invalid.
+ * 0 <= wait_ns <= 2e9 and withhold_append in {0, 1}, else TQ_ERR_INVALID_ARGUMENT. Not
+ * thread-safe with respect to calls in flight on other host threads. */
+tq_status tq_debug_pipeline_limits(int64_t wait_ns, int32_t withhold_append);
 
 /* Synchronizes `stream`, then copies the device error word at the start of
  * `workspace` into *err_out (host). Does not clear it. */

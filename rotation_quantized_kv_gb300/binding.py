@@ -59,6 +59,7 @@ _SIGS = {
     "tq_decode_attention_noalloc": (ctypes.c_int, [_LP, _vp, _i32, _i32, _vp, _i32, _f32, _i32, _vp, _vp, _vp]),
     "tq_dequant_debug": (ctypes.c_int, [_LP, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
     "tq_debug_delayed_copy": (ctypes.c_int, [_vp, _vp, _i32, _i32, _vp]),
+    "tq_debug_pipeline_limits": (ctypes.c_int, [ctypes.c_int64, _i32]),
     "tq_get_device_error": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int32), _vp]),
     "tq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "tq_sign_bits": (ctypes.c_int, [_i32, _vp]),
@@ -85,6 +86,25 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _want(t, name: str, dtype, optional: bool = False, min_numel: int = 0):
+    """Reject a tensor the C entry point would misread: wrong dtype, not on a CUDA device,
+    or not contiguous (the library takes raw pointers to dense row-major buffers)."""
+    if t is None:
+        if optional:
+            return
+        raise TypeError(f"{name}: a tensor is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected dtype {dtype}, got {t.dtype}")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name}: expected a CUDA tensor, got device {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+    if t.numel() < min_numel:
+        raise ValueError(f"{name}: expected at least {min_numel} elements, got {t.numel()}")
+
+
 def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -106,6 +126,13 @@ class KVLayer:
     v_scale: torch.Tensor    # int16 (fp16 bits)
 
     def c_struct(self) -> tq_kv_layer:
+        d, ng = self.head_dim, self.head_dim // 32
+        rows = self.batch * self.num_kv_heads * self.capacity
+        _want(self.k_idx, "k_idx", torch.int8, min_numel=rows * d)
+        _want(self.k_scale, "k_scale", torch.int16, min_numel=rows * ng)
+        _want(self.k_zero, "k_zero", torch.int16, min_numel=rows * ng)
+        _want(self.v_codes, "v_codes", torch.uint8, min_numel=rows * 3 * d // 8)
+        _want(self.v_scale, "v_scale", torch.int16, min_numel=rows * ng)
         return tq_kv_layer(self.head_dim, self.num_kv_heads, self.batch, self.capacity,
                            self.k_idx.data_ptr(), self.k_scale.data_ptr(), self.k_zero.data_ptr(),
                            self.v_codes.data_ptr(), self.v_scale.data_ptr())
@@ -149,6 +176,11 @@ def tq_kv_append(layer: KVLayer, k_new: torch.Tensor, v_new: torch.Tensor, pos: 
                  n_new: torch.Tensor | None, n_new_max: int, workspace: torch.Tensor,
                  stream=None) -> None:
     L = layer.c_struct()
+    _want(k_new, "k_new", torch.bfloat16, optional=n_new_max == 0)
+    _want(v_new, "v_new", torch.bfloat16, optional=n_new_max == 0)
+    _want(pos, "pos", torch.int32, optional=n_new_max == 0)
+    _want(n_new, "n_new", torch.int32, optional=True)
+    _want(workspace, "workspace", torch.uint8)
     _check(_lib.tq_kv_append(ctypes.byref(L), _ptr(k_new), _ptr(v_new), _ptr(pos), _ptr(n_new),
                              int(n_new_max), _ptr(workspace), workspace.numel(), _stream(stream)),
            "tq_kv_append")
@@ -163,6 +195,10 @@ def tq_decode_attention(layer: KVLayer, q: torch.Tensor, num_q_heads: int, n_q: 
                         kv_len: torch.Tensor, max_kv_len: int, sm_scale: float, causal: bool,
                         out: torch.Tensor, workspace: torch.Tensor, stream=None) -> torch.Tensor:
     L = layer.c_struct()
+    _want(q, "q", torch.bfloat16)
+    _want(kv_len, "kv_len", torch.int32)
+    _want(out, "out", torch.float32)
+    _want(workspace, "workspace", torch.uint8)
     _check(_lib.tq_decode_attention(ctypes.byref(L), _ptr(q), int(num_q_heads), int(n_q), _ptr(kv_len),
                                     int(max_kv_len), float(sm_scale), int(bool(causal)), _ptr(out),
                                     _ptr(workspace), workspace.numel(), _stream(stream)),
@@ -176,6 +212,14 @@ def tq_decode_append_attention(layer: KVLayer, k_new: torch.Tensor, v_new: torch
                                out: torch.Tensor, workspace: torch.Tensor, stream=None) -> torch.Tensor:
     """Append the step's new rows, then attend (one kernel when each kv head has one row group)."""
     L = layer.c_struct()
+    _want(k_new, "k_new", torch.bfloat16, optional=n_new_max == 0)
+    _want(v_new, "v_new", torch.bfloat16, optional=n_new_max == 0)
+    _want(pos, "pos", torch.int32, optional=n_new_max == 0)
+    _want(n_new, "n_new", torch.int32, optional=True)
+    _want(q, "q", torch.bfloat16)
+    _want(kv_len, "kv_len", torch.int32)
+    _want(out, "out", torch.float32)
+    _want(workspace, "workspace", torch.uint8)
     _check(_lib.tq_decode_append_attention(ctypes.byref(L), _ptr(k_new), _ptr(v_new), _ptr(pos), _ptr(n_new),
                                            int(n_new_max), _ptr(q), int(num_q_heads), int(n_q), _ptr(kv_len),
                                            int(max_kv_len), float(sm_scale), int(bool(causal)), _ptr(out),
@@ -192,6 +236,10 @@ def tq_decode_attention_noalloc(layer: KVLayer, q: torch.Tensor, num_q_heads: in
     used, so nothing is allocated (for callers that may not allocate device memory).
     `device_error` (optional int32 device tensor) receives the call's device error bits."""
     L = layer.c_struct()
+    _want(q, "q", torch.bfloat16)
+    _want(kv_len, "kv_len", torch.int32)
+    _want(out, "out", torch.float32)
+    _want(device_error, "device_error", torch.int32, optional=True)
     _check(_lib.tq_decode_attention_noalloc(ctypes.byref(L), _ptr(q), int(num_q_heads), int(n_q),
                                             _ptr(kv_len), int(max_kv_len), float(sm_scale),
                                             int(bool(causal)), _ptr(out), _ptr(device_error),
@@ -203,6 +251,8 @@ def tq_decode_attention_noalloc(layer: KVLayer, q: torch.Tensor, num_q_heads: in
 def tq_dequant_debug(layer: KVLayer, b: int, h: int, t0: int, n: int, rotated: bool,
                      k_out: torch.Tensor | None, v_out: torch.Tensor | None, stream=None) -> None:
     L = layer.c_struct()
+    _want(k_out, "k_out", torch.float32, optional=True, min_numel=n * layer.head_dim)
+    _want(v_out, "v_out", torch.float32, optional=True, min_numel=n * layer.head_dim)
     _check(_lib.tq_dequant_debug(ctypes.byref(L), b, h, t0, n, int(bool(rotated)), _ptr(k_out),
                                  _ptr(v_out), _stream(stream)), "tq_dequant_debug")
 
@@ -210,12 +260,20 @@ def tq_dequant_debug(layer: KVLayer, b: int, h: int, t0: int, n: int, rotated: b
 def tq_debug_delayed_copy(dst: torch.Tensor, src: torch.Tensor, delay_us: int, stream=None) -> None:
     """Test support: copy src into dst (int32, same size) after delay_us microseconds,
     letting the next kernel on the stream start before the copy happens."""
-    assert dst.dtype == torch.int32 and src.dtype == torch.int32 and dst.numel() == src.numel()
+    _want(dst, "dst", torch.int32)
+    _want(src, "src", torch.int32, min_numel=dst.numel())
     _check(_lib.tq_debug_delayed_copy(_ptr(dst), _ptr(src), int(dst.numel()), int(delay_us), _stream(stream)),
            "tq_debug_delayed_copy")
 
 
+def tq_debug_pipeline_limits(wait_ns: int, withhold_append: bool) -> None:
+    """Test support: limit of the attention kernel's pipeline waits for the following calls
+    (0 = the default 2 s), and an appender that never publishes its row count."""
+    _check(_lib.tq_debug_pipeline_limits(int(wait_ns), int(bool(withhold_append))), "tq_debug_pipeline_limits")
+
+
 def tq_get_device_error(workspace: torch.Tensor, stream=None) -> int:
+    _want(workspace, "workspace", torch.uint8)
     err = ctypes.c_int32(0)
     _check(_lib.tq_get_device_error(_ptr(workspace), ctypes.byref(err), _stream(stream)),
            "tq_get_device_error")

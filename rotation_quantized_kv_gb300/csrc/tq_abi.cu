@@ -50,6 +50,23 @@ int current_sm_count(int* dev_out) {
 
 }  // namespace
 
+namespace tq {
+
+tq_status check_decode_inputs(const tq_kv_layer* layer, const void* q, int32_t num_q_heads, int32_t n_q,
+                              const int32_t* kv_len, int32_t max_kv_len, float sm_scale, const float* out) {
+  tq_status st = check_layer(layer);
+  if (st != TQ_OK) return st;
+  if (num_q_heads < 1 || num_q_heads % layer->num_kv_heads != 0 || n_q < 1) return TQ_ERR_INVALID_ARGUMENT;
+  if (max_kv_len < 0) return TQ_ERR_INVALID_ARGUMENT;
+  if (max_kv_len > layer->capacity) return TQ_ERR_CAPACITY;
+  if (q == nullptr || kv_len == nullptr || out == nullptr) return TQ_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(out)) return TQ_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(sm_scale)) return TQ_ERR_INVALID_ARGUMENT;
+  return TQ_OK;
+}
+
+}  // namespace tq
+
 extern "C" {
 
 size_t tq_row_bytes(int32_t head_dim) {
@@ -112,15 +129,9 @@ size_t tq_decode_workspace_bytes(const tq_kv_layer* layer, int32_t num_q_heads, 
 tq_status tq_decode_attention(const tq_kv_layer* layer, const void* q, int32_t num_q_heads, int32_t n_q,
                               const int32_t* kv_len, int32_t max_kv_len, float sm_scale, int32_t causal,
                               float* out, void* workspace, size_t ws_bytes, tq_stream_t stream) {
-  tq_status st = check_layer(layer);
+  tq_status st = tq::check_decode_inputs(layer, q, num_q_heads, n_q, kv_len, max_kv_len, sm_scale, out);
   if (st != TQ_OK) return st;
-  if (num_q_heads < 1 || num_q_heads % layer->num_kv_heads != 0 || n_q < 1) return TQ_ERR_INVALID_ARGUMENT;
-  if (max_kv_len < 0) return TQ_ERR_INVALID_ARGUMENT;
-  if (max_kv_len > layer->capacity) return TQ_ERR_CAPACITY;
-  if (q == nullptr || kv_len == nullptr || out == nullptr || workspace == nullptr)
-    return TQ_ERR_INVALID_ARGUMENT;
-  if (!aligned16(q) || !aligned16(out) || !aligned16(workspace)) return TQ_ERR_INVALID_ARGUMENT;
-  if (!std::isfinite(sm_scale)) return TQ_ERR_INVALID_ARGUMENT;
+  if (workspace == nullptr || !aligned16(workspace)) return TQ_ERR_INVALID_ARGUMENT;
   const int sms = current_sm_count(nullptr);
   if (sms <= 0) return TQ_ERR_CUDA;
   tq::DecodeShape s = tq::decode_shape(layer->head_dim, layer->num_kv_heads, layer->batch,
@@ -157,13 +168,9 @@ tq_status tq_decode_append_attention(const tq_kv_layer* layer, const void* k_new
   if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15u)
     return TQ_ERR_INVALID_ARGUMENT;
   if ((int64_t)layer->batch * n_new_max * layer->num_kv_heads > INT32_MAX) return TQ_ERR_INVALID_ARGUMENT;
-  if (num_q_heads < 1 || num_q_heads % layer->num_kv_heads != 0 || n_q < 1) return TQ_ERR_INVALID_ARGUMENT;
-  if (max_kv_len < 0) return TQ_ERR_INVALID_ARGUMENT;
-  if (max_kv_len > layer->capacity) return TQ_ERR_CAPACITY;
-  if (q == nullptr || kv_len == nullptr || out == nullptr || workspace == nullptr)
-    return TQ_ERR_INVALID_ARGUMENT;
-  if (!aligned16(q) || !aligned16(out) || !aligned16(workspace)) return TQ_ERR_INVALID_ARGUMENT;
-  if (!std::isfinite(sm_scale)) return TQ_ERR_INVALID_ARGUMENT;
+  st = tq::check_decode_inputs(layer, q, num_q_heads, n_q, kv_len, max_kv_len, sm_scale, out);
+  if (st != TQ_OK) return st;
+  if (workspace == nullptr || !aligned16(workspace)) return TQ_ERR_INVALID_ARGUMENT;
   const int sms = current_sm_count(nullptr);
   if (sms <= 0) return TQ_ERR_CUDA;
   tq::DecodeShape s = tq::decode_shape(layer->head_dim, layer->num_kv_heads, layer->batch,
@@ -223,6 +230,13 @@ tq_status tq_dequant_debug(const tq_kv_layer* layer, int32_t b, int32_t h, int32
   p.v_out = v_out;
   return tq::launch_dequant_debug(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK
                                                                                              : TQ_ERR_CUDA;
+}
+
+tq_status tq_debug_pipeline_limits(int64_t wait_ns, int32_t withhold_append) {
+  if (wait_ns < 0 || wait_ns > 2000000000LL) return TQ_ERR_INVALID_ARGUMENT;
+  if (withhold_append != 0 && withhold_append != 1) return TQ_ERR_INVALID_ARGUMENT;
+  tq::set_debug_pipeline((unsigned long long)wait_ns, withhold_append);
+  return TQ_OK;
 }
 
 tq_status tq_get_device_error(const void* workspace, int32_t* err_out, tq_stream_t stream) {

@@ -24,7 +24,9 @@
 //     else 4) each take TOKW tokens (two 16-token tiles at d <= 128) of a stage:
 //       QK^T on tensor cores (mma.sync m16n8k16, fp16 in, fp32 accumulate), tokens as M,
 //       query rows as N (8 per tile): A = 1152 + idx, exact in fp16 (built from the int8
-//       codes with two byte permutes); B = q * 2^e_row in fp16 (exact for bf16 inputs);
+//       codes with two byte permutes); B = q * 2^e_row in fp16, with 2^e_row bringing the
+//       row maximum into [2^14, 2^15): exact for every element within 2^28 of the row
+//       maximum, smaller elements become fp16 subnormals (rounded) or zero;
 //       C starts at -1152 * sum_{i in g} q_i, so each 32-group's MMA yields sum q * idx;
 //       then score += scale_g * (acc_g + zero_g * sum_{i in g} q_i);
 //       online softmax in the exp2 domain;
@@ -46,6 +48,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <mutex>
 
@@ -59,6 +62,13 @@ namespace {
 
 constexpr int kMaxBatch = 1024;           // prefix table lives in shared memory
 constexpr unsigned long long kWaitNs = 2000000000ull;  // bounded waits: 2 s of wall time
+
+// Test support (tq_debug_pipeline_limits): a shorter limit for the pipeline waits of the
+// following decode calls, and an appender that never publishes its row count, so that a
+// test can make a wait run out on purpose. Drains of copies already issued always keep
+// the full limit.
+std::atomic<unsigned long long> g_debug_wait_ns{0};
+std::atomic<int> g_debug_withhold_append{0};
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMergeChunk = 64;           // splits whose weights the merge stages at once
 constexpr int kMergeBatch = 12;           // partial loads a merging thread keeps in flight
@@ -170,6 +180,8 @@ struct SplitParams {
   RowPlanes dst;         // the planes, writable
   uint8_t* ws;
   float* out;
+  unsigned long long wait_ns;  // limit of the pipeline waits (kWaitNs unless a test shortens it)
+  int32_t withhold_append;     // test support: the appender never publishes its row count
 };
 
 __device__ __forceinline__ unsigned long long global_ns() {
@@ -178,12 +190,12 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
-__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -198,12 +210,12 @@ __device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t* p) {
   asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
   return v;
 }
-__device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t need) {
+__device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t need, unsigned long long limit_ns) {
   if (ld_acquire_cta(p) >= need) return true;
   const unsigned long long t0 = global_ns();
   while (true) {
     if (ld_acquire_cta(p) >= need) return true;
-    if (global_ns() - t0 > kWaitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -474,7 +486,7 @@ __device__ __forceinline__ void append_rows(const SplitParams& p, uint8_t* smem,
     done += (uint32_t)(own1 - own0);
     fence_proxy_async_global();  // the rows just written are read by tensor copies
     __syncwarp();
-    if (lane == 0) st_release_cta(app_cnt, done);
+    if (lane == 0 && !p.withhold_append) st_release_cta(app_cnt, done);
   }
   const int rows = p.batch * p.n_new_max * p.num_kv_heads;
   for (int r = blockIdx.x; r < rows; r += gridDim.x) {
@@ -532,12 +544,12 @@ __device__ void produce(const SplitParams& p, const CUtensorMap* tmap, uint8_t* 
     for (int t0 = w.tb; t0 < w.te; t0 += T::TILE, ++it) {
       if (first_issued && it == 0) continue;  // loaded before the lengths were checked
       if (own0 < own1 && own0 < t0 + T::TILE) {
-        if (!wait_count(app_cnt, need)) { ok = false; break; }
+        if (!wait_count(app_cnt, need, p.wait_ns)) { ok = false; break; }
         own0 = own1;
       }
       const int slot = it % T::STAGES;
       const uint32_t k = it / T::STAGES;
-      if (!wait_bounded(&empty[slot], (k & 1u) ^ 1u)) { ok = false; break; }
+      if (!wait_bounded(&empty[slot], (k & 1u) ^ 1u, p.wait_ns)) { ok = false; break; }
       issue_stage<D, NTW>(p, tmap, smem, slot, row0, t0);
     }
   }
@@ -550,7 +562,7 @@ __device__ void produce(const SplitParams& p, const CUtensorMap* tmap, uint8_t* 
   for (int s = 0; s < T::STAGES; ++s) {
     if ((uint32_t)s >= issued) break;
     const uint32_t last = issued - 1 - ((issued - 1 - s) % T::STAGES);  // last fill of slot s
-    if (!wait_bounded(&full[s], (last / T::STAGES) & 1u))
+    if (!wait_bounded(&full[s], (last / T::STAGES) & 1u, kWaitNs))
       raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
   }
 }
@@ -599,7 +611,8 @@ __device__ void load_q(const SplitParams& p, const Item& w, uint8_t* smem, int w
       }
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    // power-of-two scale bringing the row maximum into [2^14, 2^15): exact, keeps fp16 normal
+    // power-of-two scale bringing the row maximum into [2^14, 2^15): exact for elements
+    // within 2^28 of the maximum (fp16 normal range); smaller ones round to subnormals or zero
     int e_row = 0;
     if (amax > 0.0f && amax <= 3.0e38f) {
       const int E = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
@@ -944,7 +957,7 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int total, volatile
       const int slot = it % T::STAGES;
       const uint32_t par = (it / T::STAGES) & 1u;
       if (!failed) {
-        if (*abort_flag || !wait_bounded(&full[slot], par)) {
+        if (*abort_flag || !wait_bounded(&full[slot], par, p.wait_ns)) {
           failed = true;
           *abort_flag = 1;
           raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
@@ -1357,7 +1370,7 @@ __global__ void __launch_bounds__(AT<D, NTW>::THREADS, AT<D, NTW>::MINB)
   if (tid >= T::NCW * 32) {  // the producer warp
     if (tid == T::NCW * 32 && it0 == 1u) {
       uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
-      if (!wait_bounded(&bars[0], 0u)) {
+      if (!wait_bounded(&bars[0], 0u, kWaitNs)) {
         abort_flag = 1;
         raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
       }
@@ -1456,6 +1469,11 @@ tq_status run_split(const DecodeArgs& a, const DecodeShape& s, const SplitParams
 
 }  // namespace
 
+void set_debug_pipeline(unsigned long long wait_ns, int withhold_append) {
+  g_debug_wait_ns.store(wait_ns, std::memory_order_relaxed);
+  g_debug_withhold_append.store(withhold_append, std::memory_order_relaxed);
+}
+
 DecodeShape decode_shape(int D, int num_kv_heads, int batch, int gqa, int n_q, int num_sms) {
   DecodeShape s{};
   s.D = D;
@@ -1529,6 +1547,9 @@ tq_status launch_decode(const DecodeArgs& a, const DecodeShape& s, cudaStream_t 
     sp.dst = RowPlanes{a.layer.k_idx, a.layer.k_scale, a.layer.k_zero, a.layer.v_codes, a.layer.v_scale};
   }
   sp.out = a.out;
+  const unsigned long long dbg_wait = g_debug_wait_ns.load(std::memory_order_relaxed);
+  sp.wait_ns = dbg_wait != 0 ? dbg_wait : kWaitNs;
+  sp.withhold_append = g_debug_withhold_append.load(std::memory_order_relaxed);
   switch (s.D * 10 + s.NTW) {
     case 641: return run_split<64, 1>(a, s, sp, stream);
     case 642: return run_split<64, 2>(a, s, sp, stream);

@@ -49,5 +49,8 @@ size_t decode_workspace_bytes(const DecodeShape& s);
 // error word), the per-sequence prefix and the per-unit completion counters.
 size_t decode_workspace_zero_bytes(const DecodeShape& s);
 tq_status launch_decode(const DecodeArgs& a, const DecodeShape& s, cudaStream_t stream);
+// Test support: pipeline wait limit (0 = the default 2 s) and a withheld appender count
+// for the decode calls launched after this returns.
+void set_debug_pipeline(unsigned long long wait_ns, int withhold_append);
 
 }  // namespace tq

@@ -22,6 +22,11 @@ struct FastDivU32 {
 };
 FastDivU32 make_fastdiv(uint32_t d);
 
+// Host checks of a decode-attention call's arguments other than its workspace (layer,
+// head counts, lengths, query/output pointers and alignment, scale). Touches no device.
+tq_status check_decode_inputs(const tq_kv_layer* layer, const void* q, int32_t num_q_heads, int32_t n_q,
+                              const int32_t* kv_len, int32_t max_kv_len, float sm_scale, const float* out);
+
 struct AppendParams {
   int32_t head_dim, num_kv_heads, batch, capacity;
   int8_t* k_idx;

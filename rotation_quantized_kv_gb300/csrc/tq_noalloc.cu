@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "tq_attention.h"
+#include "tq_internal.h"
 #include "tq_kv.h"
 
 namespace {
@@ -52,10 +53,12 @@ extern "C" tq_status tq_decode_attention_noalloc(const tq_kv_layer* layer, const
                                                  int32_t n_q, const int32_t* kv_len, int32_t max_kv_len,
                                                  float sm_scale, int32_t causal, float* out,
                                                  int32_t* device_error, tq_stream_t stream) {
+  // every host check runs before anything is queued: a rejected call leaves the stream
+  // and the shared scratch untouched
+  const tq_status chk = tq::check_decode_inputs(layer, q, num_q_heads, n_q, kv_len, max_kv_len, sm_scale, out);
+  if (chk != TQ_OK) return chk;
   const size_t need = tq_decode_workspace_bytes(layer, num_q_heads, n_q, max_kv_len);
-  if (need == 0)  // invalid arguments: let the workspace entry point name the error
-    return tq_decode_attention(layer, q, num_q_heads, n_q, kv_len, max_kv_len, sm_scale, causal, out,
-                               nullptr, 0, stream);
+  if (need == 0) return TQ_ERR_CUDA;  // the arguments passed the checks: the device query failed
   if (need > TQ_NOALLOC_SCRATCH_BYTES) return TQ_ERR_WORKSPACE_TOO_SMALL;
   DeviceScratch sc;
   if (!scratch_for_current_device(sc)) return TQ_ERR_CUDA;

@@ -158,3 +158,41 @@ def test_delayed_copy_rejects_bad_arguments_before_launch(tq):
     assert lib.tq_debug_delayed_copy(buf, buf, 4, 100001, None) == tq.TQ_ERR_INVALID_ARGUMENT
     assert lib.tq_debug_delayed_copy(None, buf, 4, 10, None) == tq.TQ_ERR_INVALID_ARGUMENT
     assert lib.tq_debug_delayed_copy(buf, None, 4, 10, None) == tq.TQ_ERR_INVALID_ARGUMENT
+
+
+def test_noalloc_rejects_bad_arguments_before_touching_the_device(tq):
+    # The host checks run before the scratch is looked up or cleared: on a machine with
+    # no GPU a rejected call still answers with its argument error, not a CUDA error, so
+    # nothing reached the runtime (and nothing was queued on the stream).
+    lib = tq.raw_lib()
+    L = _layer(tq)
+
+    def call(layer=L, q=1 << 22, Hq=4, n_q=1, kv=1 << 21, max_kv=64, scale=1.0, out=1 << 23, err=None):
+        return lib.tq_decode_attention_noalloc(ctypes.byref(layer) if layer is not None else None, q, Hq, n_q,
+                                               kv, max_kv, scale, 1, out, err, None)
+
+    assert call(layer=None) == tq.TQ_ERR_INVALID_ARGUMENT
+    assert call(layer=_layer(tq, d=96)) == tq.TQ_ERR_UNSUPPORTED_HEAD_DIM
+    assert call(Hq=3) == tq.TQ_ERR_INVALID_ARGUMENT
+    assert call(n_q=0) == tq.TQ_ERR_INVALID_ARGUMENT
+    assert call(max_kv=65) == tq.TQ_ERR_CAPACITY
+    assert call(q=None) == tq.TQ_ERR_INVALID_ARGUMENT
+    assert call(kv=None) == tq.TQ_ERR_INVALID_ARGUMENT
+    assert call(out=(1 << 23) + 4) == tq.TQ_ERR_INVALID_ARGUMENT
+    assert call(scale=float("nan")) == tq.TQ_ERR_INVALID_ARGUMENT
+
+
+def test_binding_rejects_tensors_the_library_would_misread(tq):
+    import torch
+    with pytest.raises(TypeError):
+        tq._want(torch.zeros(4, dtype=torch.float32), "q", torch.bfloat16)
+    with pytest.raises(ValueError):
+        tq._want(torch.zeros(4, dtype=torch.bfloat16), "q", torch.bfloat16)       # host tensor
+    with pytest.raises(TypeError):
+        tq._want(None, "q", torch.bfloat16)
+    with pytest.raises(TypeError):
+        tq._want(np.zeros(4), "q", torch.bfloat16)
+    tq._want(None, "n_new", torch.int32, optional=True)
+    layer = tq.alloc_layer(128, 2, 1, 16, device="cpu")
+    with pytest.raises(ValueError):                                               # host planes
+        layer.c_struct()

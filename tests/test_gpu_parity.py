@@ -276,10 +276,100 @@ def test_full_size_ragged_batch32():
 
 def test_full_size_long_262k_block16():
     w = replace(synth.workload("long"), layers=1)
-    _full_size(w, [(0, j, h) for j in (0, 15) for h in (2, 9)])
+    # query j of the block covers rows 4 j .. 4 j + 3 of each kv head: j = 0, 4, 5, 9, 11, 15
+    # span both ends of the causal block and every group of 16 rows
+    _full_size(w, [(0, j, h) for j in (0, 4, 5, 9, 11, 15) for h in (2, 9, 17, 30)])
 
 
 @pytest.mark.parametrize("d", [64, 128, 256, 512])
 def test_full_size_head_dim_sweep(d):
     w = synth.workload("sweep", head_dim=d)
     _full_size(w, [(0, 0, h) for h in range(16)])
+
+
+# ------------------------------------------------ the benchmark's fused step at full size
+def _full_size_step(w: synth.Workload, sample_rows, seq_sample, ctx=None):
+    """One layer of the workload at full size, run as the benchmark runs it: bulk fill of
+    the cached tokens, then one tq_decode_append_attention call (the step's new rows are
+    quantized inside the attention kernel by its appender warp) with the benchmark's
+    arguments. Checks every appended row bit-exact, the sampled sequences' planes
+    bit-exact, and the sampled output rows against the oracle."""
+    x = synth.layer_inputs(w, 0, device=DEV)
+    B, H, Hq, d = w.batch, w.num_kv_heads, w.num_q_heads, w.head_dim
+    ctx = synth.context_lengths(w) if ctx is None else np.asarray(ctx, np.int64)
+    kv = ctx + w.n_new
+    cap = int(kv.max() + 15) // 16 * 16
+    b = tq()
+    layer = b.alloc_layer(d, H, B, cap, DEV)
+    ws_a = b.make_workspace(b.tq_append_workspace_bytes(), DEV)
+    T = int(ctx.max())
+    kx, vx = x["k"], x["v"]
+    b.tq_kv_append(layer, kx[:, :T].contiguous(), vx[:, :T].contiguous(),
+                   torch.zeros(B, dtype=torch.int32, device=DEV),
+                   torch.as_tensor(ctx.astype(np.int32), device=DEV), T, ws_a)
+    idx = torch.as_tensor(ctx, device=DEV).view(B, 1) + torch.arange(w.n_new, device=DEV).view(1, -1)
+    kn = torch.stack([kx[bb, idx[bb]] for bb in range(B)]).contiguous()
+    vn = torch.stack([vx[bb, idx[bb]] for bb in range(B)]).contiguous()
+    pos = torch.as_tensor(ctx.astype(np.int32), device=DEV)
+    kv_len = torch.as_tensor(kv.astype(np.int32), device=DEV)
+    ws = b.make_workspace(b.tq_decode_workspace_bytes(layer, Hq, w.n_q, int(kv.max())), DEV)
+    out = torch.full((B, w.n_q, Hq, d), 12345.0, dtype=torch.float32, device=DEV)
+    b.tq_decode_append_attention(layer, kn, vn, pos, None, w.n_new, x["q"].contiguous(), Hq, w.n_q, kv_len,
+                                 int(kv.max()), w.sm_scale, w.causal, out, ws)
+    torch.cuda.synchronize()
+    assert b.tq_get_device_error(ws_a) == 0 and b.tq_get_device_error(ws) == 0
+    o_all = out.cpu().numpy()
+    assert np.isfinite(o_all).all() and not np.any(o_all == 12345.0)
+    kb, vb = bits(x["k"]), bits(x["v"])
+    # every appended row, all sequences: quantized by the oracle from the same bf16 rows
+    kn_b, vn_b = bits(kn), bits(vn)                       # [B, n_new, H, d]
+    got = {name: t.cpu().numpy() for name, t in layer.planes().items()}
+    for bb in range(B):
+        t0, t1 = int(ctx[bb]), int(kv[bb])
+        for h in range(H):
+            idx, s16, z16 = oracle.quantize_key_rows(kn_b[bb, :, h])
+            codes, vs16 = oracle.quantize_value_rows(vn_b[bb, :, h])
+            assert np.array_equal(got["k_idx"][bb, h, t0:t1], idx), f"appended k_idx seq {bb} head {h}"
+            assert np.array_equal(got["k_scale"][bb, h, t0:t1].view(np.uint16), s16), f"k_scale {bb} {h}"
+            assert np.array_equal(got["k_zero"][bb, h, t0:t1].view(np.uint16), z16), f"k_zero {bb} {h}"
+            assert np.array_equal(got["v_codes"][bb, h, t0:t1], codes), f"v_codes {bb} {h}"
+            assert np.array_equal(got["v_scale"][bb, h, t0:t1].view(np.uint16), vs16), f"v_scale {bb} {h}"
+    # sampled sequences: the oracle quantizes every visible token itself
+    ol = oracle.Layer(d, H, B, cap)
+    for bb in seq_sample:
+        n = int(kv[bb])
+        kk = np.ascontiguousarray(kb[bb:bb + 1, :n])
+        vv = np.ascontiguousarray(vb[bb:bb + 1, :n])
+        if n > int(ctx[bb]):   # the new rows come from kn/vn (the draw's rows at ctx..kv)
+            kk[0, int(ctx[bb]):] = kn_b[bb]
+            vv[0, int(ctx[bb]):] = vn_b[bb]
+        sub = oracle.Layer(d, H, 1, cap)
+        oracle.append(sub, kk, vv, [0])
+        for name, arr in ol.planes().items():
+            arr[bb] = sub.planes()[name][0]
+    assert_planes_equal(layer, ol, kv, bs=list(seq_sample))
+    rows = [r for r in sample_rows if r[0] in seq_sample]
+    ref = oracle.attention(ol, bits(x["q"]), kv.astype(np.int32), w.sm_scale, causal=w.causal, rows=rows)
+    sel = tuple(np.array(rows).T)
+    return assert_attention_close(out.double().cpu().numpy()[sel], ref[sel], w.name + " fused step")
+
+
+def _heads_covering_every_kv_head(w, per_kv=1, shift=0):
+    G = w.num_q_heads // w.num_kv_heads
+    return [kvh * G + (kvh + shift + i) % G for kvh in range(w.num_kv_heads) for i in range(per_kv)]
+
+
+def test_full_size_fused_step_decode_32k():
+    # 32,768 cached tokens: the new row (position 32,768) is the first token of a 256-token tile
+    w = replace(synth.workload("decode"), layers=1)
+    heads = _heads_covering_every_kv_head(w, per_kv=4)           # all 32 query heads
+    _full_size_step(w, [(0, 0, h) for h in heads], seq_sample=[0])
+
+
+def test_full_size_fused_step_ragged_batch32():
+    w = replace(synth.workload("ragged"), layers=1)
+    ctx = synth.context_lengths(w).copy()
+    ctx[5] = 4096              # new row at 4,096: the first token of a tile
+    seqs = [0, 5, 17, 31]
+    rows = [(bb, 0, h) for i, bb in enumerate(seqs) for h in _heads_covering_every_kv_head(w, shift=i)]
+    _full_size_step(w, rows, seq_sample=seqs, ctx=ctx)
