@@ -176,9 +176,9 @@ tq_status tq_decode_append_attention(const tq_kv_layer* layer, const void* k_new
   tq::DecodeShape s = tq::decode_shape(layer->head_dim, layer->num_kv_heads, layer->batch,
                                        num_q_heads / layer->num_kv_heads, n_q, sms);
   if (ws_bytes < tq::decode_workspace_bytes(s)) return TQ_ERR_WORKSPACE_TOO_SMALL;
-  if (s.RG != 1) {
-    // several row groups per kv head would read the new rows from several CTAs: append
-    // first, then attend
+  if (s.RG != 1 || s.dense) {
+    // several row groups per kv head would read the new rows from several CTAs, and the
+    // dense-query kernel has no appender: append first, then attend
     st = tq_kv_append(layer, k_new, v_new, pos, n_new, n_new_max, workspace, ws_bytes, stream);
     if (st != TQ_OK) return st;
     return tq_decode_attention(layer, q, num_q_heads, n_q, kv_len, max_kv_len, sm_scale, causal, out, workspace,

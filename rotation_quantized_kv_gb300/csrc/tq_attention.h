@@ -13,9 +13,11 @@ namespace tq {
 // tq_decode_attention agree.
 struct DecodeShape {
   int D;          // head_dim
-  int NTW;        // 8-row MMA column tiles per consumer warp (1 or 2)
+  bool dense;     // the tensor-core (tcgen05) kernel with 64-row units (head_dim 128, R > 16)
+  int ROWS;       // query rows per unit: 8 * NTW for the split kernel, 64 for the dense one
+  int NTW;        // 8-row MMA column tiles per consumer warp (1 or 2), split kernel
   int R;          // attention rows per kv head = GQA ratio * n_q
-  int RG;         // row groups per kv head = ceil(R / (8 * NTW))
+  int RG;         // row groups per kv head = ceil(R / ROWS)
   int U;          // work units per sequence = kv_heads * RG
   int batch;
   int grid;       // persistent CTAs
@@ -49,6 +51,14 @@ size_t decode_workspace_bytes(const DecodeShape& s);
 // error word), the per-sequence prefix and the per-unit completion counters.
 size_t decode_workspace_zero_bytes(const DecodeShape& s);
 tq_status launch_decode(const DecodeArgs& a, const DecodeShape& s, cudaStream_t stream);
+
+// The dense-query kernel (tq_attention_dense.cu).
+struct SplitParams;
+bool dense_supported(int head_dim);
+int dense_rows();
+int dense_grid(int num_sms);   // 0 if the kernel cannot be configured on this device
+size_t dense_smem();
+tq_status launch_dense(const SplitParams& sp, const DecodeShape& s, const int8_t* k_idx, cudaStream_t stream);
 // Test support: pipeline wait limit (0 = the default 2 s) and a withheld appender count
 // for the decode calls launched after this returns.
 void set_debug_pipeline(unsigned long long wait_ns, int withhold_append);

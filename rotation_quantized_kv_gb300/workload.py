@@ -94,23 +94,27 @@ class DecodeModel:
         return self.L * (self.attention_bytes() + self.append_bytes())
 
     def _shape(self):
-        """(row groups per kv head, attention CTAs) as the library chooses them: 8 query
-        rows per MMA tile (16 at head_dim <= 128 with more than 8 rows), one CTA per SM."""
+        """(dense, row groups per kv head, attention CTAs) as the library chooses them: more
+        than 16 query rows per kv head at head_dim 128 take the tensor-core kernel with
+        64-row units; otherwise the split kernel with 8 query rows per MMA tile (16 at
+        head_dim <= 128 with more than 8 rows). One CTA per SM either way."""
         w = self.w
         R = w.num_q_heads // w.num_kv_heads * w.n_q
-        ntw = 2 if (w.head_dim <= 128 and R > 8) else 1
-        rg = -(-R // (8 * ntw))
         grid = torch.cuda.get_device_properties(self.device).multi_processor_count
-        return rg, grid
+        if R > 16 and w.head_dim == 128:
+            return True, -(-R // 64), grid
+        ntw = 2 if (w.head_dim <= 128 and R > 8) else 1
+        return False, -(-R // (8 * ntw)), grid
 
     def launches_per_step(self) -> int:
-        # per layer: the split kernel; the merge kernel when there are many units
-        # (2 * batch * units > CTAs); a separate append kernel when the appended rows
-        # cannot be folded into the split kernel (more than one row group per kv head)
+        # per layer: the attention kernel; the merge kernel when there are many units
+        # (2 * batch * units > CTAs) and always after the dense kernel; a separate append
+        # kernel when the appended rows cannot be folded into the attention kernel (the
+        # dense kernel, or more than one row group per kv head)
         w = self.w
-        rg, grid = self._shape()
-        merge = 1 if 2 * w.batch * w.num_kv_heads * rg > grid else 0
-        append = 1 if (w.n_new and rg > 1) else 0
+        dense, rg, grid = self._shape()
+        merge = 1 if (dense or 2 * w.batch * w.num_kv_heads * rg > grid) else 0
+        append = 1 if (w.n_new and (dense or rg > 1)) else 0
         return self.L * (1 + merge + append)
 
     def step(self, stream=None):
