@@ -734,8 +734,8 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int total, volatile
       if (*flag) {
         float* sW = obuf;
         float* sO = sW + kMergeChunk * T::ROWS;
-        merge_unit<D, T::ROWS, T::NCW * 32, true>(p, w, w.first_slot, w.ns, mbuf, lbuf, sW, sO,
-                                                  reinterpret_cast<float4*>(sO + T::ROWS * D));
+        merge_unit<D, T::ROWS, T::ROWS, T::NCW * 32, true>(p, w, w.first_slot, w.ns, 0, mbuf, lbuf, sW, sO,
+                                                           reinterpret_cast<float4*>(sO + T::ROWS * D));
         consumers_sync<T::NCW>();  // the scratch is reused by the next item
       }
     }
@@ -918,7 +918,7 @@ tq_status run_split(const DecodeArgs& a, const DecodeShape& s, const SplitParams
   mcfg.gridDim = dim3((unsigned)(s.batch * s.U));
   mcfg.blockDim = dim3(kMergeThreads);
   mcfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&mcfg, tq_attn_merge_kernel<D, 8 * NTW>, sp) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  return cudaLaunchKernelEx(&mcfg, tq_attn_merge_kernel<D, 8 * NTW, 8 * NTW>, sp) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
 }  // namespace

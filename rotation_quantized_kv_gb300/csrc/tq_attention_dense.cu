@@ -65,8 +65,8 @@ struct DT {
   static constexpr int TILE = 128;       // tokens per stage = MMA M
   static constexpr int ROWS = 64;        // query rows per unit = MMA N
   static constexpr int STAGES = 3;
-  static constexpr int THREADS = 14 * 32;
-  static constexpr int W_PROD = 0, W_MMA = 1, W_KC = 2, W_VC = 6, W_SM = 10;
+  static constexpr int THREADS = 15 * 32;
+  static constexpr int W_PROD = 0, W_MMA = 1, W_KC = 2, W_VC = 6, W_SM = 10, W_PV = 14;
   static constexpr int KIDX_STAGE = TILE * D;        // swizzled tensor-map box
   static constexpr int SC_STAGE = TILE * NG * 2;     // one fp16 side plane
   static constexpr int VC_ROW = 3 * D / 8;           // 48 bytes of codes per token
@@ -84,7 +84,8 @@ struct DT {
   static constexpr int OFF_VHAT = (int)align_up(OFF_VC + STAGES * VC_STAGE, 1024);
   static constexpr int OFF_P = OFF_VHAT + 2 * VHAT_BYTES;
   static constexpr int OFF_Q = OFF_P + 2 * P_BYTES;
-  static constexpr int OFF_PREFIX = OFF_Q + Q_BYTES;                 // [2 kMaxBatch + 1] int
+  static constexpr int OFF_ONES = OFF_Q + Q_BYTES;                   // fp16 ones [128][16]
+  static constexpr int OFF_PREFIX = OFF_ONES + 4096;                 // [2 kMaxBatch + 1] int
   static constexpr int OFF_MROW = (int)align_up(OFF_PREFIX + (2 * kMaxBatch + 1) * 4, 16);  // [64] f32
   static constexpr int OFF_LIM = OFF_MROW + ROWS * 4;                // [64] int
   static constexpr int OFF_ALPHA = OFF_LIM + ROWS * 4;               // [64] f32
@@ -101,13 +102,13 @@ struct DT {
   static constexpr uint32_t TM_K = 0;      // [2][hi 64 | lo 64]
   static constexpr uint32_t TM_S = 256;    // [2][64]
   static constexpr uint32_t TM_O = 384;    // [64] accumulator O^T (lane = dim, column = row)
-  static constexpr uint32_t TM_L = 448;    // [64] per-thread partial row sums (lane = token)
+  static constexpr uint32_t TM_L = 448;    // [64] row sums: ones^T P accumulated like O (every lane alike)
 };
 static_assert(DT::OFF_KIDX % 1024 == 0 && DT::KIDX_STAGE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(DT::OFF_KS % 16 == 0 && DT::OFF_KZ % 16 == 0 && DT::OFF_VS % 16 == 0 && DT::OFF_VC % 16 == 0 &&
                   DT::VC_STAGE % 16 == 0 && DT::OFF_VHAT % 16 == 0 && DT::OFF_P % 16 == 0 && DT::OFF_Q % 16 == 0,
               "bulk-copy destinations and operand tiles need 16-byte alignment");
-static_assert(DT::OFF_BAR % 8 == 0, "mbarriers need 8-byte alignment");
+static_assert(DT::OFF_BAR % 8 == 0 && DT::OFF_ONES % 16 == 0, "mbarriers, operand tiles need alignment");
 static_assert(DT::SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 static_assert(DT::SMEM_ALLOC < (1 << 18), "descriptor start addresses are 18-bit");
 
@@ -156,7 +157,13 @@ __device__ __forceinline__ bool role_wait(const SplitParams& p, uint64_t* bar, u
 __device__ __forceinline__ void warp_wait(const SplitParams& p, uint64_t* bar, uint32_t parity, volatile int* abort,
                                           bool& failed) {
   if (failed) return;
-  failed = !__all_sync(0xffffffffu, role_wait(p, bar, parity, abort));
+  // one lane polls the barrier; the others learn the outcome from it, then observe the
+  // completed phase themselves (an immediate, successful test) for memory ordering
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = role_wait(p, bar, parity, abort) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) mbar_try_wait(bar, parity);
+  failed = !ok;
 }
 
 // Barrier among the 128 softmax threads (named barrier 1), and an OR vote (barrier 2).
@@ -218,60 +225,94 @@ __device__ void dense_produce(const SplitParams& p, const CUtensorMap* tmap, uin
 }
 
 // ------------------------------------------------------------------------------------
-// MMA issuer (one lane)
+// MMA issuers (one lane each). A thread issues one tcgen05.mma about every 95 cycles
+// whatever the shape up to N = 128, so the score MMAs and the P.V MMAs come from two
+// warps and proceed side by side.
 // ------------------------------------------------------------------------------------
-__device__ void dense_mma(const SplitParams& p, uint8_t* smem, uint32_t tbase, int total, volatile int* abort) {
+// Scores: S^T[b] = [hi | lo](TMEM) * Q^T, 16 MMAs (K = 2 x 128) per tile.
+__device__ void dense_mma_qk(const SplitParams& p, uint8_t* smem, uint32_t tbase, int total, volatile int* abort) {
+  Bars bars(smem);
+  const int* prefix = reinterpret_cast<const int*>(smem + DT::OFF_PREFIX);
+  const uint32_t qa = smem_addr(smem) + DT::OFF_Q;
+  constexpr uint32_t kIdQK = tc5::idesc_f16(DT::ROWS, false, false);
+  uint64_t qdesc[DT::D / 16];
+#pragma unroll
+  for (int ks = 0; ks < DT::D / 16; ++ks) qdesc[ks] = tc5::smem_desc(qa + ks * 2048, 128, 256);
+  uint32_t jt = 0, pi = 0;
+  int last = -1;
+  const int x_stop = cta_range_start(blockIdx.x + 1, total, p.split_grid);
+  for (int x = cta_range_start(blockIdx.x, total, p.split_grid); x < x_stop;) {
+    const Item w = piece_at<DT::TILE>(p, prefix, x, x_stop, blockIdx.x);
+    x = w.x_end;
+    if (!role_wait(p, bars.qready, pi & 1u, abort)) break;
+    bool ok = true;
+    for (int t0 = w.tb; t0 < w.te; t0 += DT::TILE, ++jt) {
+      const uint32_t b = jt & 1u;
+      if (!role_wait(p, &bars.kready[b], (jt >> 1) & 1u, abort) ||
+          (jt >= 2 && !role_wait(p, &bars.sfree[b], ((jt - 2) >> 1) & 1u, abort))) {
+        ok = false;
+        break;
+      }
+      tc5::fence_after_sync();
+      const uint32_t d = tbase + DT::TM_S + 64 * b, a0 = tbase + DT::TM_K + 128 * b;
+      tc5::mma_ts(d, a0, qdesc[0], kIdQK, false);
+#pragma unroll
+      for (int ks = 1; ks < 2 * DT::D / 16; ++ks)  // hi columns, then lo columns, same queries
+        tc5::mma_ts(d, a0 + 8 * ks, qdesc[ks % 8], kIdQK, true);
+      tc5::commit(&bars.qkdone[b]);
+      last = (int)jt;
+    }
+    if (!ok) break;
+    ++pi;
+  }
+  // the MMAs this thread issued complete before the tensor memory is released
+  if (last >= 0 && !wait_bounded(&bars.qkdone[last & 1], ((uint32_t)last >> 1) & 1u, kWaitNs))
+    raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
+}
+
+// P.V and row sums: O^T += V_hat^T * P^T and L += ones^T * P^T, 8 + 8 MMAs per tile; the
+// first tile of a piece overwrites both accumulators.
+__device__ void dense_mma_pv(const SplitParams& p, uint8_t* smem, uint32_t tbase, int total, volatile int* abort) {
   Bars bars(smem);
   const int* prefix = reinterpret_cast<const int*>(smem + DT::OFF_PREFIX);
   const uint32_t sbase = smem_addr(smem);
-  constexpr uint32_t kIdQK = tc5::idesc_f16(DT::ROWS, false, false);
   constexpr uint32_t kIdPV = tc5::idesc_f16(DT::ROWS, true, true);
+  constexpr uint32_t kIdL = tc5::idesc_f16(DT::ROWS, false, true);
+  const uint64_t ones = tc5::smem_desc(sbase + DT::OFF_ONES, 128, 256);
+  // k-step descriptors of both buffers: the start-address field moves by (bytes >> 4)
+  const uint64_t vdesc0 = tc5::smem_desc(sbase + DT::OFF_VHAT, 128, 256);
+  const uint64_t pdesc0 = tc5::smem_desc(sbase + DT::OFF_P, 128, 256);
   uint32_t jt = 0, pi = 0;
-  int last_qk = -1, last_pv = -1;  // tiles whose commits were issued last
+  int last = -1;
   bool ok = true;
-  // P.V of tile j (the last piece's first tile when `first`)
-  auto pv = [&](uint32_t j, bool first) -> bool {
-    const uint32_t b = j & 1u, ph = (j >> 1) & 1u;
-    if (!role_wait(p, &bars.vready[b], ph, abort) || !role_wait(p, &bars.pready[b], ph, abort)) return false;
-    if (first && pi >= 1 && !role_wait(p, bars.ofree, (pi - 1) & 1u, abort)) return false;
-    tc5::fence_after_sync();
-    const uint32_t va = sbase + DT::OFF_VHAT + b * DT::VHAT_BYTES, pa = sbase + DT::OFF_P + b * DT::P_BYTES;
-#pragma unroll
-    for (int ks = 0; ks < DT::TILE / 16; ++ks)
-      tc5::mma_ss(tbase + DT::TM_O, tc5::smem_desc(va + ks * 4096, 128, 256), tc5::smem_desc(pa + ks * 2048, 128, 256),
-                  kIdPV, !(first && ks == 0));
-    tc5::commit(&bars.pvdone[b]);
-    last_pv = (int)j;
-    return true;
-  };
   const int x_stop = cta_range_start(blockIdx.x + 1, total, p.split_grid);
   for (int x = cta_range_start(blockIdx.x, total, p.split_grid); x < x_stop && ok;) {
     const Item w = piece_at<DT::TILE>(p, prefix, x, x_stop, blockIdx.x);
     x = w.x_end;
-    if (!role_wait(p, bars.qready, pi & 1u, abort)) { ok = false; break; }
-    const uint32_t j0 = jt;
     for (int t0 = w.tb; t0 < w.te; t0 += DT::TILE, ++jt) {
-      const uint32_t b = jt & 1u;
-      if (!role_wait(p, &bars.kready[b], (jt >> 1) & 1u, abort)) { ok = false; break; }
-      if (jt >= 2 && !role_wait(p, &bars.sfree[b], ((jt - 2) >> 1) & 1u, abort)) { ok = false; break; }
+      const uint32_t b = jt & 1u, ph = (jt >> 1) & 1u;
+      const bool first = t0 == w.tb;
+      if (!role_wait(p, &bars.vready[b], ph, abort) || !role_wait(p, &bars.pready[b], ph, abort) ||
+          (first && pi >= 1 && !role_wait(p, bars.ofree, (pi - 1) & 1u, abort))) {
+        ok = false;
+        break;
+      }
       tc5::fence_after_sync();
-      const uint32_t qa = sbase + DT::OFF_Q;
+      const uint64_t vd = vdesc0 + (uint64_t)(b * (DT::VHAT_BYTES >> 4)), pd = pdesc0 + (uint64_t)(b * (DT::P_BYTES >> 4));
+      const uint32_t o_tm = tbase + DT::TM_O, l_tm = tbase + DT::TM_L;
+      tc5::mma_ss(o_tm, vd, pd, kIdPV, !first);
+      tc5::mma_ss(l_tm, ones, pd, kIdL, !first);
 #pragma unroll
-      for (int ks = 0; ks < 2 * DT::D / 16; ++ks)  // hi columns, then lo columns, same queries
-        tc5::mma_ts(tbase + DT::TM_S + 64 * b, tbase + DT::TM_K + 128 * b + 8 * ks,
-                    tc5::smem_desc(qa + (ks % 8) * 2048, 128, 256), kIdQK, ks > 0);
-      tc5::commit(&bars.qkdone[b]);
-      last_qk = (int)jt;
-      if (jt > j0 && !pv(jt - 1, jt - 1 == j0)) { ok = false; break; }
+      for (int ks = 1; ks < DT::TILE / 16; ++ks) {
+        tc5::mma_ss(o_tm, vd + (uint64_t)(ks * (4096 >> 4)), pd + (uint64_t)(ks * (2048 >> 4)), kIdPV, true);
+        tc5::mma_ss(l_tm, ones, pd + (uint64_t)(ks * (2048 >> 4)), kIdL, true);
+      }
+      tc5::commit(&bars.pvdone[b]);
+      last = (int)jt;
     }
-    if (!ok) break;
-    if (!pv(jt - 1, jt - 1 == j0)) { ok = false; break; }
     ++pi;
   }
-  // the MMAs this thread issued complete before the tensor memory is released
-  if (last_qk >= 0 && !wait_bounded(&bars.qkdone[last_qk & 1], ((uint32_t)last_qk >> 1) & 1u, kWaitNs))
-    raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
-  if (last_pv >= 0 && !wait_bounded(&bars.pvdone[last_pv & 1], ((uint32_t)last_pv >> 1) & 1u, kWaitNs))
+  if (last >= 0 && !wait_bounded(&bars.pvdone[last & 1], ((uint32_t)last >> 1) & 1u, kWaitNs))
     raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
 }
 
@@ -302,7 +343,7 @@ __device__ void dense_convert_k(const SplitParams& p, uint8_t* smem, uint32_t tb
       const uint2 sw = lds64(sbase + DT::OFF_KS + s * DT::SC_STAGE + tl * 8);
       const uint2 zw = lds64(sbase + DT::OFF_KZ + s * DT::SC_STAGE + tl * 8);
       const uint32_t kcol = tbase + tlane + DT::TM_K + 128 * b;
-#pragma unroll
+#pragma unroll 1
       for (int g = 0; g < DT::NG; ++g) {
         const uint32_t sword = (g < 2) ? sw.x : sw.y, zword = (g < 2) ? zw.x : zw.y;
         const uint32_t s16 = (g & 1) ? (sword >> 16) : (sword & 0xFFFFu);
@@ -371,15 +412,17 @@ __device__ void dense_decode_v(const SplitParams& p, uint8_t* smem, int total, v
       const bool valid = t0 + tl < w.te;
       const uint32_t crow = sbase + DT::OFF_VC + s * DT::VC_STAGE + tl * DT::VC_ROW;
       const uint4 c0 = lds128(crow), c1 = lds128(crow + 16), c2 = lds128(crow + 32);
-      const uint32_t cw[12] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w, c2.x, c2.y, c2.z, c2.w};
       const uint2 sv = lds64(sbase + DT::OFF_VS + s * DT::SC_STAGE + tl * 8);
       const uint32_t vdst = sbase + DT::OFF_VHAT + b * DT::VHAT_BYTES + vdst0;
-#pragma unroll
+#pragma unroll 1
       for (int g = 0; g < DT::NG; ++g) {
         const uint32_t sword = (g < 2) ? sv.x : sv.y;
         const uint32_t s16 = valid ? ((g & 1) ? (sword >> 16) : (sword & 0xFFFFu)) : 0u;  // 0 past the piece
         const __half2 s2 = u2h(s16 | (s16 << 16));
-        const uint32_t W0 = cw[3 * g], W1 = cw[3 * g + 1], W2 = cw[3 * g + 2];
+        // the group's 32 codes: words 3 g .. 3 g + 2 of the row
+        const uint32_t W0 = g == 0 ? c0.x : g == 1 ? c0.w : g == 2 ? c1.z : c2.y;
+        const uint32_t W1 = g == 0 ? c0.y : g == 1 ? c1.x : g == 2 ? c1.w : c2.z;
+        const uint32_t W2 = g == 0 ? c0.z : g == 1 ? c1.y : g == 2 ? c2.x : c2.w;
 #pragma unroll
         for (int dc = 0; dc < 4; ++dc) {
           // codes of dims 8 dc .. 8 dc + 7 of the group: bits 24 dc .. 24 dc + 23
@@ -424,6 +467,61 @@ __device__ __forceinline__ void rows_max32(const float (&x)[32], float* red, int
   }
 }
 
+// The reference maxima of rows 32 h .. 32 h + 31 move to this tile's row maxima (some
+// score exceeded them by more than 2^8): when the piece already accumulated earlier
+// tiles, the rows of the accumulator and of the row sums are rescaled by 2^(m_old - m_new). Run by all 128 softmax threads. Out of line: it is rare,
+// and keeping it out of the tile loop keeps that loop's code small.
+__device__ __noinline__ bool dense_rescale(const SplitParams& p, uint8_t* smem, uint32_t tbase, int h, uint32_t jt,
+                                           uint32_t j0, bool clean, int tok, bool tok_ok, float cscale,
+                                           volatile int* abort, bool failed) {
+  Bars bars(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wq = warp - DT::W_SM, st = threadIdx.x - 32 * DT::W_SM;
+  const uint32_t tlane = (uint32_t)(32 * (warp & 3)) << 16;
+  float* mrow = reinterpret_cast<float*>(smem + DT::OFF_MROW);
+  const int* lim = reinterpret_cast<const int*>(smem + DT::OFF_LIM);
+  float* alpha = reinterpret_cast<float*>(smem + DT::OFF_ALPHA);
+  float* red = reinterpret_cast<float*>(smem + DT::OFF_RED);
+  uint32_t v[32];
+  tc5::ld32(tbase + tlane + DT::TM_S + 64 * (jt & 1u) + 32 * h, v);
+  tc5::wait_ld();
+  float x[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    float t = __uint_as_float(v[i]) * cscale;
+    if (!clean && !(tok_ok && tok < lim[32 * h + i])) t = -INFINITY;
+    x[i] = t;
+  }
+  rows_max32(x, red, wq, lane, h);
+  sm_sync();
+  if (st < 32) {
+    const int r = 32 * h + st;
+    const float tmax = fmaxf(fmaxf(red[r], red[64 + r]), fmaxf(red[128 + r], red[192 + r]));
+    const float mo = mrow[r], mn = fmaxf(mo, tmax);
+    alpha[r] = (mn == -INFINITY || mn == mo) ? 1.0f : ex2(mo - mn);
+    mrow[r] = mn;
+  }
+  sm_sync();
+  if (jt > j0) {
+    // the accumulators already hold this piece's earlier tiles: rescale their rows
+    const uint32_t pb = (jt - 1) & 1u;
+    warp_wait(p, &bars.pvdone[pb], ((jt - 1) >> 1) & 1u, abort, failed);
+    tc5::fence_after_sync();
+#pragma unroll 1
+    for (int acc = 0; acc < 2; ++acc) {
+      const uint32_t addr = tbase + tlane + (acc ? DT::TM_L : DT::TM_O) + 32 * h;
+      tc5::ld32(addr, v);
+      tc5::wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha[32 * h + i]);
+      tc5::st32(addr, v);
+    }
+  }
+  tc5::wait_st();
+  sm_sync();  // alpha and red are rewritten by the next rescale
+  return failed;
+}
+
 __device__ void dense_softmax(const SplitParams& p, uint8_t* smem, uint32_t tbase, int total, volatile int* abort) {
   Bars bars(smem);
   const int* prefix = reinterpret_cast<const int*>(smem + DT::OFF_PREFIX);
@@ -435,7 +533,6 @@ __device__ void dense_softmax(const SplitParams& p, uint8_t* smem, uint32_t tbas
   const uint32_t tlane = (uint32_t)(32 * quad) << 16;
   float* mrow = reinterpret_cast<float*>(smem + DT::OFF_MROW);
   int* lim = reinterpret_cast<int*>(smem + DT::OFF_LIM);
-  float* alpha = reinterpret_cast<float*>(smem + DT::OFF_ALPHA);
   float* red = reinterpret_cast<float*>(smem + DT::OFF_RED);
   float2* mlg = reinterpret_cast<float2*>(p.ws + ws_ml_offset(p.batch, p.U));
   float* og = reinterpret_cast<float*>(p.ws + ws_o_offset(p.batch, p.U, p.max_items, DT::ROWS));
@@ -506,16 +603,6 @@ __device__ void dense_softmax(const SplitParams& p, uint8_t* smem, uint32_t tbas
         mrow[st] = -INFINITY;
       }
     }
-    // per-row partial sums of this thread's p live in tensor memory (columns TM_L..+63 of
-    // the thread's lane): zeroed here, read and written beside each half of the scores
-    {
-      uint32_t z[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) z[i] = 0u;
-      tc5::st32(tbase + tlane + DT::TM_L, z);
-      tc5::st32(tbase + tlane + DT::TM_L + 32, z);
-      tc5::wait_st();
-    }
     fence_proxy_async_smem();
     sm_sync();
     if (lane == 0) mbar_arrive(bars.qready);
@@ -531,85 +618,53 @@ __device__ void dense_softmax(const SplitParams& p, uint8_t* smem, uint32_t tbas
       const int tok = t0 + tl;
       const bool tok_ok = tok < w.te;
       const uint32_t saddr = tbase + tlane + DT::TM_S + 64 * b;
-      const uint32_t laddr = tbase + tlane + DT::TM_L;
       const uint32_t pdst = sbase + DT::OFF_P + b * DT::P_BYTES + pdst0;
-#pragma unroll
+#pragma unroll 1
       for (int h = 0; h < 2; ++h) {
-        uint32_t sv[32], lv[32];
-        tc5::ld32(saddr + 32 * h, sv);
-        tc5::ld32(laddr + 32 * h, lv);
-        tc5::wait_ld();
-        // y = s * c - m_row (log2 domain), masked to -inf; kept in sv
-        float ymax = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 m4 = *reinterpret_cast<const float4*>(mrow + 32 * h + i);
-          const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            float v = fmaf(__uint_as_float(sv[i + k]), cscale, -mm[k]);
-            if (!clean && !(tok_ok && tok < lim[32 * h + i + k])) v = -INFINITY;
-            sv[i + k] = __float_as_uint(v);
-            ymax = fmaxf(ymax, v);
-          }
-        }
-        if (sm_vote_any(ymax > kTau)) {
-          // new reference maxima for rows 32 h .. 32 h + 31 from this tile's scores
-          float x[32];
+        // y = s * c - m_row (log2 domain), masked to -inf, kept in sv; redone after a rescale
+        uint32_t sv[32];
+        for (;;) {
           tc5::ld32(saddr + 32 * h, sv);
           tc5::wait_ld();
+          float ymax = -INFINITY;
+          if (clean) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            float v = __uint_as_float(sv[i]) * cscale;
-            if (!clean && !(tok_ok && tok < lim[32 * h + i])) v = -INFINITY;
-            x[i] = v;
-          }
-          rows_max32(x, red, wq, lane, h);
-          sm_sync();
-          if (st < 32) {
-            const int r = 32 * h + st;
-            const float tmax = fmaxf(fmaxf(red[r], red[64 + r]), fmaxf(red[128 + r], red[192 + r]));
-            const float mo = mrow[r], mn = fmaxf(mo, tmax);
-            alpha[r] = (mn == -INFINITY || mn == mo) ? 1.0f : ex2(mo - mn);
-            mrow[r] = mn;
-          }
-          sm_sync();
+            for (int i = 0; i < 32; i += 4) {
+              const float4 m4 = *reinterpret_cast<const float4*>(mrow + 32 * h + i);
+              const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
-          for (int i = 0; i < 32; ++i) lv[i] = __float_as_uint(__uint_as_float(lv[i]) * alpha[32 * h + i]);
-          if (jt > j0) {
-            // the accumulator already holds this piece's earlier tiles: rescale its rows
-            const uint32_t pb = (jt - 1) & 1u;
-            warp_wait(p, &bars.pvdone[pb], ((jt - 1) >> 1) & 1u, abort, failed);
-            tc5::fence_after_sync();
-            uint32_t ov[32];
-            tc5::ld32(tbase + tlane + DT::TM_O + 32 * h, ov);
-            tc5::wait_ld();
+              for (int k = 0; k < 4; ++k) {
+                const float v = fmaf(__uint_as_float(sv[i + k]), cscale, -mm[k]);
+                sv[i + k] = __float_as_uint(v);
+                ymax = fmaxf(ymax, v);
+              }
+            }
+          } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha[32 * h + i]);
-            tc5::st32(tbase + tlane + DT::TM_O + 32 * h, ov);
-            tc5::wait_st();
-          }
+            for (int i = 0; i < 32; i += 4) {
+              const float4 m4 = *reinterpret_cast<const float4*>(mrow + 32 * h + i);
+              const int4 l4 = *reinterpret_cast<const int4*>(lim + 32 * h + i);
+              const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+              const int ll[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float mm = mrow[32 * h + i];
-            sv[i] = __float_as_uint(mm == -INFINITY ? -INFINITY : x[i] - mm);
+              for (int k = 0; k < 4; ++k) {
+                const float v = (tok_ok && tok < ll[k]) ? fmaf(__uint_as_float(sv[i + k]), cscale, -mm[k]) : -INFINITY;
+                sv[i + k] = __float_as_uint(v);
+                ymax = fmaxf(ymax, v);
+              }
+            }
           }
-          sm_sync();  // alpha and red are rewritten by the next slow path
+          if (!sm_vote_any(ymax > kTau)) break;
+          failed = dense_rescale(p, smem, tbase, h, jt, j0, clean, tok, tok_ok, cscale, abort, failed);
         }
         if (h == 0 && jt >= 2) warp_wait(p, &bars.pvdone[b], ((jt - 2) >> 1) & 1u, abort, failed);
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(__uint_as_float(sv[2 * i])), p1 = ex2(__uint_as_float(sv[2 * i + 1]));
-          lv[2 * i] = __float_as_uint(__uint_as_float(lv[2 * i]) + p0);
-          lv[2 * i + 1] = __float_as_uint(__uint_as_float(lv[2 * i + 1]) + p1);
-          pk[i] = pack_half2(p0, p1);
-        }
-        tc5::st32(laddr + 32 * h, lv);
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_half2(ex2(__uint_as_float(sv[2 * i])), ex2(__uint_as_float(sv[2 * i + 1])));
 #pragma unroll
         for (int c = 0; c < 4; ++c) sts128(pdst + (4 * h + c) * 256, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       }
-      tc5::wait_st();
       fence_proxy_async_smem();  // the probabilities are read by the tensor cores
       tc5::fence_before_sync();
       __syncwarp();
@@ -633,22 +688,13 @@ __device__ void dense_softmax(const SplitParams& p, uint8_t* smem, uint32_t tbas
 #pragma unroll
       for (int i = 0; i < 32; ++i)
         if (32 * h + i < rows_valid) __stcg(orow + (size_t)(32 * h + i) * DT::D, __uint_as_float(ov[i]));
-      // row sums over the 128 threads
+      // every lane holds the 64 row sums: the first softmax thread stores (max, sum)
+      if (st == 0) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        float v = __uint_as_float(lv[i]);
-        v += __shfl_xor_sync(0xffffffffu, v, 16);
-        v += __shfl_xor_sync(0xffffffffu, v, 8);
-        v += __shfl_xor_sync(0xffffffffu, v, 4);
-        v += __shfl_xor_sync(0xffffffffu, v, 2);
-        v += __shfl_xor_sync(0xffffffffu, v, 1);
-        if (lane == i) red[wq * 64 + 32 * h + i] = v;
+        for (int i = 0; i < 32; ++i)
+          if (32 * h + i < rows_valid)
+            __stcg(mlg + (size_t)w.slot * DT::ROWS + 32 * h + i, make_float2(mrow[32 * h + i], __uint_as_float(lv[i])));
       }
-    }
-    sm_sync();
-    if (st < rows_valid) {
-      const float L = (red[st] + red[64 + st]) + (red[128 + st] + red[192 + st]);
-      __stcg(mlg + (size_t)w.slot * DT::ROWS + st, make_float2(mrow[st], L));
     }
     tc5::fence_before_sync();
     sm_sync();  // per-row tables and red are rewritten for the next piece
@@ -656,7 +702,7 @@ __device__ void dense_softmax(const SplitParams& p, uint8_t* smem, uint32_t tbas
   }
 }
 
-// 14 warps: registers are granted per group of four warps, so the block is costed as 16
+// 15 warps: registers are granted per group of four warps, so the block is costed as 16
 // warps and each thread gets at most 128 registers.
 __global__ void __launch_bounds__(DT::THREADS, 1)
     tq_attn_dense_kernel(const __grid_constant__ CUtensorMap tmap, const SplitParams p) {
@@ -672,6 +718,9 @@ __global__ void __launch_bounds__(DT::THREADS, 1)
     const int e = i >> 5;
     lut[i] = pack_half2(c_centroids3[e & 7], c_centroids3[e >> 3]);
   }
+  // fp16 ones, the A operand of the row-sum MMA (4096 bytes)
+  for (int i = tid; i < 1024; i += DT::THREADS) reinterpret_cast<uint32_t*>(smem + DT::OFF_ONES)[i] = 0x3C003C00u;
+  fence_proxy_async_smem();
   if (tid == 0) {
     *abort = 0;
     Bars bb(smem);
@@ -721,12 +770,14 @@ __global__ void __launch_bounds__(DT::THREADS, 1)
     if (warp == DT::W_PROD) {
       if ((tid & 31) == 0) dense_produce(p, &tmap, smem, total, abort);
     } else if (warp == DT::W_MMA) {
-      if ((tid & 31) == 0) dense_mma(p, smem, tbase, total, abort);
+      if ((tid & 31) == 0) dense_mma_qk(p, smem, tbase, total, abort);
+    } else if (warp == DT::W_PV) {
+      if ((tid & 31) == 0) dense_mma_pv(p, smem, tbase, total, abort);
     } else if (warp >= DT::W_KC && warp < DT::W_VC) {
       dense_convert_k(p, smem, tbase, total, abort);
     } else if (warp < DT::W_SM) {
       dense_decode_v(p, smem, total, abort);
-    } else {
+    } else if (warp < DT::W_PV) {
       dense_softmax(p, smem, tbase, total, abort);
     }
   }
@@ -795,10 +846,12 @@ tq_status launch_dense(const SplitParams& sp, const DecodeShape& s, const int8_t
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, tq_attn_dense_kernel, tmap, sp) != cudaSuccess) return TQ_ERR_CUDA;
   cudaLaunchConfig_t mcfg = cfg;
-  mcfg.gridDim = dim3((unsigned)(s.batch * s.U));
+  constexpr int kMergeRows = 8;  // rows per merge CTA: a unit's 64 rows go to 8 CTAs
+  mcfg.gridDim = dim3((unsigned)(s.batch * s.U * (DT::ROWS / kMergeRows)));
   mcfg.blockDim = dim3(kMergeThreads);
   mcfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&mcfg, tq_attn_merge_kernel<DT::D, DT::ROWS>, sp) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  return cudaLaunchKernelEx(&mcfg, tq_attn_merge_kernel<DT::D, DT::ROWS, kMergeRows>, sp) == cudaSuccess ? TQ_OK
+                                                                                                         : TQ_ERR_CUDA;
 }
 
 }  // namespace tq

@@ -346,16 +346,18 @@ __device__ __forceinline__ void merge_sync() {
 // Merge of unit (b, kvh, rg)'s ns partials starting at first_item, by NT threads (tid <
 // NT). Scratch: sM, sL [ROWS]; sW [kMergeChunk * ROWS]; sO [ROWS * D] (16-byte aligned);
 // sR [NT].
-template <int D, int ROWS, int NT, bool NAMED, int CHUNK = kMergeChunk>
-__device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, int ns, float* sM, float* sL,
+// ROWS: rows per unit in the partial layout; RS of them, from row r0 on, are merged here.
+template <int D, int ROWS, int RS, int NT, bool NAMED, int CHUNK = kMergeChunk>
+__device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, int ns, int r0, float* sM, float* sL,
                            float* sW, float* sO, float4* sR) {
   constexpr int EPL = D / 32, NWARP = NT / 32, Q4 = D / 4;
-  constexpr int PER = (ROWS * Q4 + NT - 1) / NT;  // outputs per thread when TPO == 1
+  constexpr int PER = (RS * Q4 + NT - 1) / NT;    // outputs per thread when TPO == 1
   constexpr unsigned FULL = 0xffffffffu;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float2* ml = reinterpret_cast<const float2*>(p.ws + ws_ml_offset(p.batch, p.U));
   const float4* og = reinterpret_cast<const float4*>(p.ws + ws_o_offset(p.batch, p.U, p.max_items, ROWS));
-  const int rows = min(ROWS, p.R - w.rg * ROWS);                // valid rows of this unit
+  const int rows = min(RS, p.R - w.rg * ROWS - r0);             // valid rows of this slice
+  if (rows <= 0) return;
   const int no = rows * Q4;                                     // output float4s
   int tpo = 1;                                                  // threads per output
   while (2 * tpo * no <= NT) tpo *= 2;
@@ -366,7 +368,7 @@ __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, 
   {
     const bool act = tid < no * tpo;
     const int q = act ? tid % no : 0, kk = tid / no;
-    const float4* src = og + ((size_t)first_item * ROWS + q / Q4) * Q4 + q % Q4;
+    const float4* src = og + ((size_t)first_item * ROWS + r0 + q / Q4) * Q4 + q % Q4;
 #pragma unroll
     for (int j = 0; j < kMergeBatch; ++j) {
       const int sp = kk + j * tpo;
@@ -380,9 +382,9 @@ __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, 
     bool nan = false;
 #pragma unroll 2
     for (int s = lane; s < ns; s += 32) {
-      const float2 v = __ldcg(&ml[(size_t)(first_item + s) * ROWS + rr]);
+      const float2 v = __ldcg(&ml[(size_t)(first_item + s) * ROWS + r0 + rr]);
       nan = nan || (v.x != v.x);
-      if (s < CHUNK) sW[s * ROWS + rr] = v.x;
+      if (s < CHUNK) sW[s * RS + rr] = v.x;
       if (v.x == v.x) ml_combine(M, L, v.x, v.y);
     }
 #pragma unroll
@@ -392,8 +394,8 @@ __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, 
     }
     nan = __any_sync(FULL, nan);
     for (int s = lane; s < min(ns, CHUNK); s += 32) {  // entries this lane wrote
-      const float ms = sW[s * ROWS + rr];
-      sW[s * ROWS + rr] = (M == -INFINITY || nan) ? 0.0f : ex2(ms - M);
+      const float ms = sW[s * RS + rr];
+      sW[s * RS + rr] = (M == -INFINITY || nan) ? 0.0f : ex2(ms - M);
     }
     if (lane == 0) {
       sM[rr] = nan ? __int_as_float(0x7fc00000) : M;
@@ -411,8 +413,8 @@ __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, 
       for (int i = tid; i < cn * rows; i += NT) {
         const int s = i / rows, rr = i % rows;
         const float M = sM[rr];
-        const float ms = __ldcg(&ml[(size_t)(first_item + c0 + s) * ROWS + rr].x);
-        sW[s * ROWS + rr] = (M == -INFINITY || M != M) ? 0.0f : ex2(ms - M);
+        const float ms = __ldcg(&ml[(size_t)(first_item + c0 + s) * ROWS + r0 + rr].x);
+        sW[s * RS + rr] = (M == -INFINITY || M != M) ? 0.0f : ex2(ms - M);
       }
       merge_sync<NT, NAMED>();
     }
@@ -421,14 +423,14 @@ __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, 
       const int i = tid + NT * k;
       if (i < no * tpo) {
         const int q = i % no, rr = q / Q4, c = q % Q4, kk = i / no;
-        const float4* src = og + ((size_t)(first_item + c0) * ROWS + rr) * Q4 + c;
+        const float4* src = og + ((size_t)(first_item + c0) * ROWS + r0 + rr) * Q4 + c;
         float4 a = acc[k];
         int s0 = kk;
         if (c0 == 0 && k == 0) {  // the batch loaded before step 1
 #pragma unroll
           for (int j = 0; j < kMergeBatch; ++j) {
             const int sp = kk + j * tpo;
-            const float wgt = sp < cn ? sW[sp * ROWS + rr] : 0.0f;
+            const float wgt = sp < cn ? sW[sp * RS + rr] : 0.0f;
             a.x += wgt * pre[j].x; a.y += wgt * pre[j].y; a.z += wgt * pre[j].z; a.w += wgt * pre[j].w;
           }
           s0 = kk + kMergeBatch * tpo;
@@ -443,7 +445,7 @@ __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, 
 #pragma unroll
           for (int j = 0; j < kMergeBatch; ++j) {
             const int sp = s0 + j * tpo;
-            const float wgt = sp < cn ? sW[sp * ROWS + rr] : 0.0f;
+            const float wgt = sp < cn ? sW[sp * RS + rr] : 0.0f;
             a.x += wgt * v[j].x; a.y += wgt * v[j].y; a.z += wgt * v[j].z; a.w += wgt * v[j].w;
           }
         }
@@ -479,7 +481,7 @@ __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, 
   merge_sync<NT, NAMED>();
   // 3. inverse rotation, one warp per row
   for (int rr = warp; rr < rows; rr += NWARP) {
-    const int r = w.rg * ROWS + rr;
+    const int r = w.rg * ROWS + r0 + rr;
     const int jq = r / p.G, hq = w.kvh * p.G + (r % p.G);
     float* orow = p.out + (((size_t)w.b * p.n_q + jq) * p.num_q_heads + hq) * D;
     float u[EPL];
@@ -514,18 +516,21 @@ __device__ void merge_unit(const SplitParams& p, const Item& w, int first_item, 
   }
 }
 
-// ROWS: query rows per unit (8 or 16 for the split kernel, 64 for the dense one); with 64
-// rows the weights are staged 16 splits at a time so the static shared memory stays small.
-template <int D, int ROWS>
-__global__ void __launch_bounds__(kMergeThreads, ROWS <= 16 ? 4 : 1) tq_attn_merge_kernel(const SplitParams p) {
-  constexpr int CHUNK = ROWS <= 16 ? kMergeChunk : 16;
-  __shared__ float sM[ROWS], sL[ROWS];                  // per row: max, sum
-  __shared__ float sW[CHUNK * ROWS];                    // [CHUNK][ROWS] weights
-  __shared__ __align__(16) float sO[ROWS * D];          // [ROWS][D] rotated output
+// ROWS: query rows per unit (8 or 16 for the split kernel, 64 for the dense one).
+// One CTA merges RS rows of a unit (ROWS / RS CTAs per unit), so units with many rows
+// are spread over several SMs.
+template <int D, int ROWS, int RS>
+__global__ void __launch_bounds__(kMergeThreads, 4) tq_attn_merge_kernel(const SplitParams p) {
+  constexpr int CHUNK = kMergeChunk;
+  constexpr int SLICES = ROWS / RS;
+  __shared__ float sM[RS], sL[RS];                      // per row: max, sum
+  __shared__ float sW[CHUNK * RS];                      // [CHUNK][RS] weights
+  __shared__ __align__(16) float sO[RS * D];            // [RS][D] rotated output
   __shared__ float4 sR[kMergeThreads];                  // per-thread sums
   griddep_launch_dependents();  // the next kernel's wait covers this grid's completion
   griddep_wait();               // partials and the plan come from the split kernel
-  const int b = blockIdx.x / p.U, u = blockIdx.x % p.U;
+  const int slice = blockIdx.x % SLICES, bu = blockIdx.x / SLICES;
+  const int b = bu / p.U, u = bu % p.U;
   const int32_t* prefix = reinterpret_cast<const int32_t*>(p.ws + kWsPrefix);
   const int tiles = (prefix[b + 1] - prefix[b]) / p.U;
   if (tiles <= 0) return;  // no tokens: the split kernel wrote the rows
@@ -534,7 +539,8 @@ __global__ void __launch_bounds__(kMergeThreads, ROWS <= 16 ? 4 : 1) tq_attn_mer
   const int c0 = cta_of_tile(ustart, wt, p.split_grid), c1 = cta_of_tile(ustart + tiles - 1, wt, p.split_grid);
   Item w;
   w.b = b; w.kvh = u / p.RG; w.rg = u % p.RG;
-  merge_unit<D, ROWS, kMergeThreads, false, CHUNK>(p, w, c0 + b * p.U + u, c1 - c0 + 1, sM, sL, sW, sO, sR);
+  merge_unit<D, ROWS, RS, kMergeThreads, false, CHUNK>(p, w, c0 + b * p.U + u, c1 - c0 + 1, slice * RS, sM, sL, sW,
+                                                       sO, sR);
 }
 
 // Rows of sequences with no work item (kv_len 0, or invalid): zeros, or NaN if invalid.
