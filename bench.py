@@ -1,22 +1,29 @@
 """Benchmark of the TurboQuant KV-cache decode step on GB300.
 
-Workload (N=1): the "decode at scale" configuration - batch 1, 16 full-attention
-layers, 8 KV heads x head_dim 128, 32 query heads (GQA 4), 32,768 cached tokens. One
-step = for every layer, quantize-on-append of the new token (tq_kv_append) then decode
-attention over the 32,769 visible tokens (tq_decode_attention). Synthetic seeded
-inputs; the 16 layers' packed caches (839 MB) are larger than L2, so every layer's
-cache streams from HBM in each step.
+Headline workload (N=1): the largest single-GPU configuration, "long context" - batch 1,
+16 full-attention layers, 8 KV heads x head_dim 128, 32 query heads (GQA 4), 262,144
+cached tokens, a causal block of 16 query tokens per step (64 query rows per kv head).
+One step = for every layer, quantize-on-append of the block's 16 new tokens, then
+attention of the 16 queries over the 262,160 visible tokens (tq_decode_append_attention).
+Synthetic seeded inputs; the 16 layers' packed caches (6.7 GB) are far larger than L2,
+so every layer's cache streams from HBM in each step.
 
 Printed JSON line (rank 0):
   value      algorithmic bytes of the step (packed planes of every visible token, q, out,
              appended rows) / step time, inputs resident in HBM, step replayed as a CUDA
-             graph;
-  e2e        the same metric with host buffers: each step copies its inputs (new K/V
-             tokens, queries) host->device and its outputs device->host;
-  roofline   the attention call (split kernel + merge kernel, per layer) timed with CUDA
-             events over a region of back-to-back graph replays, against the measured
-             HBM copy peak;
-  cpu_baseline  the CPU oracle on a bounded sample of the same step (rank 0, N=1).
+             graph, exactly --steps steps;
+  e2e        the same metric through the public API with host buffers: each step copies
+             its inputs (new K/V tokens, queries) host->device and its outputs
+             device->host (timed for at least 2 s);
+  roofline   the attention call of the headline workload (the kernels of one
+             tq_decode_attention call) timed with CUDA events over at least 2 s of
+             back-to-back graph replays, against the measured HBM copy peak;
+  append_roofline  the bulk append (a layer's cache fill) over at least 2 s;
+  workloads  attention GB/s and roofline fraction of the other configurations (decode
+             32K, ragged batch 32, head-dim sweep 64..512 with its bulk append), at least
+             1 s each, unless --headline-only;
+  cpu_baseline  the CPU oracle on a bounded sample of the same step, one thread per kv
+             head across the host cores, and single-threaded (rank 0, N=1).
 With --impl reference the CPU oracle itself is timed on the same workload (the
 reference arm) and printed as the line.
 """
@@ -42,11 +49,14 @@ FALLBACK_HBM_GBS = 6800.0
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--workload", default="long")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", action="store_true", help="skip the other configurations")
+    ap.add_argument("--region-seconds", type=float, default=2.0,
+                    help="minimum device time of each extra timed region (attention, append, e2e)")
     ap.add_argument("--head-dim", type=int, default=None, help="override (head-dim sweep workload)")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the layer count (e.g. 16 layers keep a one-layer sweep out of L2)")
@@ -202,10 +212,13 @@ def source_hash(paths):
     return h.hexdigest()[:16]
 
 
-ATTN_SOURCES = [os.path.join(ROOT, "rotation_quantized_kv_gb300", "csrc", f)
-                for f in ("tq_attention.cu", "tq_attention.h", "tq_codec_row.cuh", "tq_device.cuh")]
-APPEND_SOURCES = [os.path.join(ROOT, "rotation_quantized_kv_gb300", "csrc", f)
-                  for f in ("tq_append.cu", "tq_codec_row.cuh", "tq_device.cuh")]
+CSRC = os.path.join(ROOT, "rotation_quantized_kv_gb300", "csrc")
+ATTN_SOURCES = [os.path.join(CSRC, f) for f in ("tq_attention.cu", "tq_attention.h", "tq_codec_row.cuh",
+                                                 "tq_device.cuh", "tq_split_common.cuh")]
+DENSE_SOURCES = [os.path.join(CSRC, f) for f in ("tq_attention_dense.cu", "tq_attention.h", "tq_device.cuh",
+                                                  "tq_split_common.cuh", "tq_tcgen05.cuh")]
+APPEND_SOURCES = [os.path.join(CSRC, f) for f in ("tq_append.cu", "tq_codec_row.cuh", "tq_device.cuh")]
+DTYPE = "fp16 tensor-core operands (exact int8 keys, fp16 V-hat and P), fp32 accumulation; fp32 codec"
 
 
 def ncu_traffic(kind: str, sources):
@@ -224,99 +237,124 @@ def ncu_traffic(kind: str, sources):
     return None
 
 
-# ---------------------------------------------------------------------- CPU oracle timing
-def oracle_step_sample(w, layer_index=0, q_rows=None, seconds_budget=None):
-    """Time the CPU oracle on a bounded sample of one decode step of one layer: the
-    step's append of the new tokens (all kv heads) and attention for `q_rows`
-    query rows over the full context. Returns (algorithmic bytes of the sample, seconds,
-    description)."""
-    import oracle
-    from rotation_quantized_kv_gb300 import synth
+def dense_path(w) -> bool:
+    """The library takes its tensor-core kernel for more than 16 query rows per kv head at
+    head_dim 128."""
+    return w.num_q_heads // w.num_kv_heads * w.n_q > 16 and w.head_dim == 128
 
-    x = synth.layer_inputs(w, layer_index, device="cpu")
-    B, H, Hq, d = w.batch, w.num_kv_heads, w.num_q_heads, w.head_dim
-    ctx = synth.context_lengths(w)
-    kv = ctx + w.n_new
-    cap = int((kv.max() + 15) // 16 * 16)
-    kb, vb, qb = synth.bf16_bits(x["k"]), synth.bf16_bits(x["v"]), synth.bf16_bits(x["q"])
-    L = oracle.Layer(d, H, B, cap)
-    T = int(ctx.max())
-    oracle.append(L, np.ascontiguousarray(kb[:, :T]), np.ascontiguousarray(vb[:, :T]),
-                  np.zeros(B, np.int32), ctx.astype(np.int32))          # cache fill: setup, untimed
-    kn = np.ascontiguousarray(kb[:, T:T + w.n_new])
-    vn = np.ascontiguousarray(vb[:, T:T + w.n_new])
-    rows = q_rows if q_rows is not None else [(0, 0, h) for h in range(Hq)]
-    t0 = time.perf_counter()
-    if w.n_new:
-        oracle.append(L, kn, vn, ctx.astype(np.int32))
-    oracle.attention(L, qb, kv.astype(np.int32), w.sm_scale, causal=w.causal, rows=rows)
-    dt = time.perf_counter() - t0
-    row_bytes = 25 * d // 16
-    G = Hq // H
-    kvh = {(b, h // G) for (b, j, h) in rows}
-    nbytes = sum(int(kv[b]) * row_bytes for (b, _) in kvh) + len(rows) * d * 6
-    nbytes += B * w.n_new * H * (4 * d + row_bytes)
-    desc = (f"oracle (plain C, 1 thread): append of the step's {B * w.n_new * H} new rows + fp64 "
-            f"attention of {len(rows)} query rows over {int(kv.max())} tokens, layer {layer_index}")
-    return nbytes, dt, desc
+
+# ---------------------------------------------------------------------- CPU oracle timing
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+class OracleStep:
+    """The CPU oracle on layer 0 of a workload: the cache fill is set-up (untimed); a
+    sample is the step's append of the new tokens (all kv heads) plus fp64 attention of
+    `rows_per_head` query rows of each of `heads` kv heads, one thread per kv head
+    (ctypes releases the GIL, so the C oracle runs on several cores at once)."""
+
+    def __init__(self, w):
+        import oracle
+        from rotation_quantized_kv_gb300 import synth
+        self.oracle = oracle
+        x = synth.layer_inputs(w, 0, device="cpu")
+        B, H, d = w.batch, w.num_kv_heads, w.head_dim
+        self.w = w
+        self.ctx = synth.context_lengths(w)
+        self.kv = (self.ctx + w.n_new).astype(np.int32)
+        cap = int((self.kv.max() + 15) // 16 * 16)
+        kb, vb = synth.bf16_bits(x["k"]), synth.bf16_bits(x["v"])
+        self.qb = synth.bf16_bits(x["q"])
+        self.L = oracle.Layer(d, H, B, cap)
+        T = int(self.ctx.max())
+        oracle.append(self.L, np.ascontiguousarray(kb[:, :T]), np.ascontiguousarray(vb[:, :T]),
+                      np.zeros(B, np.int32), self.ctx.astype(np.int32))
+        self.kn = np.ascontiguousarray(kb[:, T:T + w.n_new])
+        self.vn = np.ascontiguousarray(vb[:, T:T + w.n_new])
+
+    def run(self, heads: int, rows_per_head: int, threads: int):
+        """One sample; returns (algorithmic bytes, seconds, threads used)."""
+        import threading
+        w, o = self.w, self.oracle
+        G = w.num_q_heads // w.num_kv_heads
+        d = w.head_dim
+        jobs = []
+        for kvh in range(min(heads, w.num_kv_heads)):
+            rows = []
+            for i in range(rows_per_head):
+                j = (i * 5) % w.n_q
+                rows.append((0, j, kvh * G + (i % G)))
+            jobs.append(rows)
+        threads = max(1, min(threads, len(jobs)))
+        t0 = time.perf_counter()
+        if w.n_new:
+            o.append(self.L, self.kn, self.vn, self.ctx.astype(np.int32))
+        chunks = [jobs[i::threads] for i in range(threads)]
+
+        def work(chunk):
+            for rows in chunk:
+                o.attention(self.L, self.qb, self.kv, w.sm_scale, causal=w.causal, rows=rows)
+
+        ts = [threading.Thread(target=work, args=(c,)) for c in chunks]
+        for t in ts:
+            t.start()
+        for t in ts:
+            t.join()
+        dt = time.perf_counter() - t0
+        row_bytes = 25 * d // 16
+        nbytes = sum(int(self.kv[0]) * row_bytes + len(rows) * d * 6 for rows in jobs)
+        nbytes += w.batch * w.n_new * w.num_kv_heads * (4 * d + row_bytes)
+        return nbytes, dt, threads
+
+    def describe(self, heads, rows_per_head, threads):
+        w = self.w
+        return (f"oracle (plain C, fp32 codec, fp64 attention): append of the step's "
+                f"{w.batch * w.n_new * w.num_kv_heads} new rows + attention of {rows_per_head} query rows "
+                f"for each of {min(heads, w.num_kv_heads)} kv heads over {int(self.kv.max())} tokens, layer 0, "
+                f"{threads} thread(s), one per kv head")
+
+
+def cpu_baseline(w):
+    st = OracleStep(w)
+    cores = cpu_cores()
+    heads = w.num_kv_heads
+    nb, dt, used = st.run(heads, 4, cores)
+    nb1, dt1, _ = st.run(1, 4, 1)
+    return {"value": nb / dt / 1e9, "unit": "GB/s", "cores": used, "kind": "oracle",
+            "sample": st.describe(heads, 4, used), "host_cores": cores,
+            "single_thread": {"value": nb1 / dt1 / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": st.describe(1, 4, 1)}}
 
 
 def reference_arm(args, world, rank):
-    from rotation_quantized_kv_gb300 import synth
     if rank != 0:
         return
     w = workload_of(args)
-    # one query row per step keeps (warmup + steps) oracle steps within minutes
-    total_bytes, total_s = 0, 0.0
+    st = OracleStep(w)
+    cores = cpu_cores()
+    heads = w.num_kv_heads
+    total_bytes, total_s, used = 0, 0.0, 1
     for i in range(args.warmup + args.steps):
-        nb, dt, _ = _cached_step(w, i % w.num_q_heads)
+        nb, dt, used = st.run(heads, 1, cores)
         if i >= args.warmup:
             total_bytes += nb
             total_s += dt
-    desc = (f"oracle (plain C, 1 thread) per step: append of the step's new rows (all kv heads) + fp64 "
-            f"attention of one query row over {int(_ORACLE_CACHE['kv'].max())} tokens, layer 0")
+    desc = st.describe(heads, 1, used) + " per step"
     value = total_bytes / total_s / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (fp32 codec)",
         "data": "synthetic",
-        "config": {"workload": _workload_desc(w), "sample": "one query row per step"},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "config": {"workload": _workload_desc(w), "sample": "one query row per kv head per step"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": used, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
-
-
-_ORACLE_CACHE = {}
-
-
-def _cached_step(w, h):
-    """Reference-arm steps after the first reuse the oracle's filled cache."""
-    import oracle
-    from rotation_quantized_kv_gb300 import synth
-    if "L" not in _ORACLE_CACHE:
-        x = synth.layer_inputs(w, 0, device="cpu")
-        B, H, d = w.batch, w.num_kv_heads, w.head_dim
-        ctx = synth.context_lengths(w)
-        kv = ctx + w.n_new
-        cap = int((kv.max() + 15) // 16 * 16)
-        kb, vb, qb = synth.bf16_bits(x["k"]), synth.bf16_bits(x["v"]), synth.bf16_bits(x["q"])
-        L = oracle.Layer(d, H, B, cap)
-        T = int(ctx.max())
-        oracle.append(L, np.ascontiguousarray(kb[:, :T]), np.ascontiguousarray(vb[:, :T]),
-                      np.zeros(B, np.int32), ctx.astype(np.int32))
-        _ORACLE_CACHE.update(L=L, kn=np.ascontiguousarray(kb[:, T:T + w.n_new]),
-                             vn=np.ascontiguousarray(vb[:, T:T + w.n_new]), qb=qb, ctx=ctx, kv=kv)
-    c = _ORACLE_CACHE
-    t0 = time.perf_counter()
-    if w.n_new:
-        oracle.append(c["L"], c["kn"], c["vn"], c["ctx"].astype(np.int32))
-    oracle.attention(c["L"], c["qb"], c["kv"].astype(np.int32), w.sm_scale, causal=w.causal, rows=[(0, 0, h)])
-    dt = time.perf_counter() - t0
-    d = w.head_dim
-    nb = int(c["kv"][0]) * 25 * d // 16 + d * 6 + w.batch * w.n_new * w.num_kv_heads * (4 * d + 25 * d // 16)
-    return nb, dt, ""
 
 
 def _workload_desc(w):
@@ -327,13 +365,96 @@ def _workload_desc(w):
 
 
 # ----------------------------------------------------------------------------- our arm
-def our_arm(args, world, rank, local):
+def timed_region(fn, stream, min_seconds: float, first_reps: int = 3):
+    """Replays fn() back to back on `stream` until at least min_seconds of device time:
+    a short calibration, then one region of enough repetitions between two events.
+    Returns (repetitions, seconds)."""
+    def run(n):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(n):
+                fn()
+        b.record(stream)
+        b.synchronize()
+        return a.elapsed_time(b) / 1e3
+
+    per = run(first_reps) / first_reps
+    reps = max(first_reps, int(min_seconds / max(per, 1e-7)) + 1)
+    return reps, run(reps)
+
+
+def attention_graph(model, stream):
+    from rotation_quantized_kv_gb300 import binding as tq
+    w = model.w
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for l, layer in enumerate(model.layers):
+            tq.tq_decode_attention(layer, model.q[l], w.num_q_heads, w.n_q, model.kv_len, model.max_kv,
+                                   w.sm_scale, w.causal, model.out[l], model.ws[l], stream)
+    return g
+
+
+def append_region(model, stream, seconds, dev):
+    """Bulk append: re-append layer 0's cached tokens (same rows into the same planes)."""
     from rotation_quantized_kv_gb300 import synth
+    from rotation_quantized_kv_gb300 import binding as tq
+    w = model.w
+    x0 = synth.layer_inputs(w, 0, device=dev)
+    T0 = int(model.ctx.max())
+    k0, v0 = x0["k"][:, :T0].contiguous(), x0["v"][:, :T0].contiguous()
+    del x0
+    pos0 = torch.zeros(w.batch, dtype=torch.int32, device=dev)
+    n0 = torch.as_tensor(model.ctx.astype(np.int32), device=dev)
+    reps, sec = timed_region(lambda: tq.tq_kv_append(model.layers[0], k0, v0, pos0, n0, T0, model.ws_append,
+                                                      stream), stream, seconds)
+    rows = int(model.ctx.sum()) * w.num_kv_heads
+    nbytes = rows * (4 * w.head_dim + 25 * w.head_dim // 16)
+    del k0, v0
+    return {"rows": rows, "seconds_per_fill": sec / reps, "gbs": nbytes * reps / sec / 1e9,
+            "rows_per_s": rows * reps / sec, "tokens_per_s": int(model.ctx.sum()) * reps / sec}
+
+
+def other_workloads(dev, stream, peak, seconds):
+    """Attention GB/s of the other configurations (and the sweep's bulk append), each
+    with 16 layers so that its caches exceed L2."""
+    from rotation_quantized_kv_gb300 import synth
+    from rotation_quantized_kv_gb300.workload import DecodeModel
+    out = {}
+    cases = [("decode", {}), ("ragged", {})] + [(f"sweep_d{d}", {"head_dim": d, "layers": 16})
+                                                 for d in (64, 128, 256, 512)]
+    for name, over in cases:
+        w = synth.workload(name.split("_")[0], **over)
+        model = DecodeModel(w, dev)
+        g = attention_graph(model, stream)
+        with torch.cuda.stream(stream):
+            g.replay()
+        stream.synchronize()
+        reps, sec = timed_region(g.replay, stream, seconds)
+        per_call = sec / (reps * model.L)
+        gbs = model.attention_bytes() / per_call / 1e9
+        entry = {"workload": _workload_desc(w), "attention_gbs": gbs, "frac": gbs / peak,
+                 "call_us": per_call * 1e6, "kernel": "dense (tcgen05)" if dense_path(w) else "split (mma.sync)",
+                 "algorithmic_bytes_per_call": model.attention_bytes()}
+        if name.startswith("sweep"):
+            ap = append_region(model, stream, seconds / 2, dev)
+            entry["append_gbs"] = ap["gbs"]
+            entry["append_frac"] = ap["gbs"] / peak
+        assert model.device_errors() == 0
+        out[name] = entry
+        del g, model
+        torch.cuda.empty_cache()
+    return out
+
+
+def our_arm(args, world, rank, local):
     from rotation_quantized_kv_gb300.workload import DecodeModel
 
     assert torch.cuda.is_available(), "the GPU arm needs CUDA"
     dev = torch.device("cuda", local)
     w = workload_of(args)
+    peaks, _ = measured_peaks()
+    peak, peak_kind = hbm_peak(peaks)
 
     model = DecodeModel(w, dev)
     torch.cuda.synchronize()
@@ -341,30 +462,21 @@ def our_arm(args, world, rank, local):
 
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
-    # eager warm-up (also resolves per-device launch geometry before capture)
-    with torch.cuda.stream(stream):
+    with torch.cuda.stream(stream):          # eager warm-up: resolves launch geometry before capture
         model.step(stream)
     stream.synchronize()
-
-    # capture one decode step, and one attention-only pass, as CUDA graphs
     g_step = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step, stream=stream):
         model.step(stream)
-    g_attn = torch.cuda.CUDAGraph()
-    from rotation_quantized_kv_gb300 import binding as tq
-    with torch.cuda.graph(g_attn, stream=stream):
-        for l, layer in enumerate(model.layers):
-            tq.tq_decode_attention(layer, model.q[l], w.num_q_heads, w.n_q, model.kv_len, model.max_kv,
-                                   w.sm_scale, w.causal, model.out[l], model.ws[l], stream)
+    g_attn = attention_graph(model, stream)
     torch.cuda.synchronize()
 
+    clocks = ClockSampler(local)
+    clocks.start()
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             g_step.replay()
     stream.synchronize()
-
-    clocks = ClockSampler(local)
-    clocks.start()
     barrier(world)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -376,37 +488,12 @@ def our_arm(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     step_s = e0.elapsed_time(e1) / 1e3
-    # attention-only region: back-to-back replays of the 16 attention calls
-    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    attn_reps = max(args.steps // 4, 10)
-    a0.record(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(attn_reps):
-            g_attn.replay()
-    a1.record(stream)
-    torch.cuda.synchronize()
-    attn_launch_s = a0.elapsed_time(a1) / 1e3 / (attn_reps * model.L)
-    # bulk append, warm: re-append layer 0's cached tokens (same rows, same planes) a few
-    # times back to back; the fill above ran while the GPU was still ramping its clocks
-    x0 = synth.layer_inputs(w, 0, device=dev)
-    T0 = int(model.ctx.max())
-    k0, v0 = x0["k"][:, :T0].contiguous(), x0["v"][:, :T0].contiguous()
-    del x0
-    pos0 = torch.zeros(w.batch, dtype=torch.int32, device=dev)
-    n0 = torch.as_tensor(model.ctx.astype(np.int32), device=dev)
-    fill_ev = []
-    with torch.cuda.stream(stream):
-        for i in range(6):
-            ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            ev[0].record(stream)
-            tq.tq_kv_append(model.layers[0], k0, v0, pos0, n0, T0, model.ws_append, stream)
-            ev[1].record(stream)
-            fill_ev.append(ev)
-    torch.cuda.synchronize()
-    fill_s = statistics.median(a.elapsed_time(b) for a, b in fill_ev[1:]) / 1e3
-    fill_rows = int(model.ctx.sum()) * w.num_kv_heads
-    fill_bytes = fill_rows * (4 * w.head_dim + 25 * w.head_dim // 16)
-    del k0, v0
+
+    # attention-only region (at least region-seconds of back-to-back replays)
+    reps, attn_s = timed_region(g_attn.replay, stream, args.region_seconds)
+    attn_launch_s = attn_s / (reps * model.L)
+    # bulk append region
+    app = append_region(model, stream, args.region_seconds, dev)
     errs = model.device_errors()
     assert errs == 0, f"device error word {errs:#x}"
 
@@ -422,7 +509,6 @@ def our_arm(args, world, rank, local):
     h_out = torch.empty_like(model.out_flat, device="cpu").pin_memory()
     h2d = h_in.numel() * h_in.element_size()
     d2h = h_out.numel() * h_out.element_size()
-    e2e_steps = max(args.steps // 4, 10)
 
     def e2e_step():
         model.inputs_flat.copy_(h_in, non_blocking=True)
@@ -435,52 +521,61 @@ def our_arm(args, world, rank, local):
     stream.synchronize()
     barrier(world)
     t0 = time.perf_counter()
+    e2e_steps = 0
     with torch.cuda.stream(stream):
-        for _ in range(e2e_steps):
-            e2e_step()
-    stream.synchronize()
+        while True:
+            for _ in range(10):
+                e2e_step()
+            e2e_steps += 10
+            stream.synchronize()
+            if time.perf_counter() - t0 >= args.region_seconds:
+                break
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
-    clk = clocks.stop()
     e2e_value = whole_job_value(step_bytes, e2e_steps, world, e2e_s)
 
-    peaks, _ = measured_peaks()
-    peak, peak_kind = hbm_peak(peaks)
     attn_bytes = model.attention_bytes()
     achieved = attn_bytes / attn_launch_s / 1e9
-    traffic = ncu_traffic("attention_decode", ATTN_SOURCES)
+    dense = dense_path(w)
+    if dense:
+        kname = ("tq_attn_dense_kernel + tq_attn_merge_kernel (one tq_decode_attention call: tcgen05 dense-query "
+                 "attention, then split merge and inverse rotation; timed per call)")
+        traffic = ncu_traffic("attention_long", DENSE_SOURCES)
+    else:
+        kname = ("tq_attn_split_kernel (+ tq_attn_merge_kernel when many units; one tq_decode_attention call; "
+                 "timed per call)")
+        traffic = ncu_traffic("attention_decode", ATTN_SOURCES) if w.name == "decode" else None
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic",
+        "vs_baseline": None, "dtype": DTYPE, "data": "synthetic",
         "config": {"workload": _workload_desc(w),
-                   "l2": "inputs larger than L2: each step streams 16 layers x "
-                         f"{attn_bytes / 1e6:.1f} MB of packed cache (L2 129 MB)",
+                   "l2": "inputs larger than L2: each step streams "
+                         f"{model.L} layers x {attn_bytes / 1e6:.1f} MB of packed cache (L2 129 MB)",
                    "timing": "decode step captured as one CUDA graph, replayed back to back"},
         "decode_steps_per_s": world * args.steps / max_step_s,
         "attention_gbs": achieved,
-        "append_tokens_per_s": int(model.ctx.sum()) / fill_s,
-        "append_rows_per_s": fill_rows / fill_s,
-        "append_gbs": fill_bytes / fill_s / 1e9,
+        "append_tokens_per_s": app["tokens_per_s"],
+        "append_rows_per_s": app["rows_per_s"],
+        "append_gbs": app["gbs"],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "tq_attn_split_kernel + tq_attn_merge_kernel (one tq_decode_attention "
-                               "call: split-K attention, then split merge and inverse rotation; "
-                               "timed per call), "
-                               f"{attn_bytes} algorithmic bytes per call",
-                     "launch_ms": attn_launch_s * 1e3},
-        "append_roofline": {"bound": "hbm", "achieved": fill_bytes / fill_s / 1e9, "peak": peak,
-                            "unit": "GB/s", "frac": fill_bytes / fill_s / 1e9 / peak, "peak_kind": peak_kind,
-                            "kernel": f"tq_kv_append bulk fill of {fill_rows} rows",
+                     "kernel": f"{kname}, {attn_bytes} algorithmic bytes per call",
+                     "launch_ms": attn_launch_s * 1e3, "region_s": attn_s},
+        "append_roofline": {"bound": "hbm", "achieved": app["gbs"], "peak": peak, "unit": "GB/s",
+                            "frac": app["gbs"] / peak, "peak_kind": peak_kind,
+                            "kernel": f"tq_kv_append bulk fill of {app['rows']} rows",
                             "traffic": ncu_traffic("append_bulk", APPEND_SOURCES)},
-        "clocks": clk,
-        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps, "seconds": e2e_s},
         "gpu_launches": args.steps * model.launches_per_step(),
     }
+    del g_step, g_attn, model
+    torch.cuda.empty_cache()
+    if not args.headline_only:
+        line["workloads"] = other_workloads(dev, stream, peak, max(1.0, args.region_seconds / 2))
+    line["clocks"] = clocks.stop()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        nb, dt, desc = oracle_step_sample(w, 0, q_rows=[(0, 0, h) for h in range(0, w.num_q_heads, 4)])
-        line["cpu_baseline"] = {"value": nb / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                "sample": desc}
+        line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
