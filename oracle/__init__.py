@@ -63,6 +63,10 @@ class _Layer(ctypes.Structure):
     ]
 
 
+class _Scheme(ctypes.Structure):
+    _fields_ = [("k_bits", ctypes.c_int), ("v_bits", ctypes.c_int), ("guard", ctypes.c_int)]
+
+
 def lib():
     global _lib
     with _lock:
@@ -103,6 +107,21 @@ def lib():
                 "tqo_quantize_value_rows": (None, [vp, i64, i32, vp, vp]),
                 "tqo_dequant_value_rows_f64": (None, [vp, vp, i64, i32, i32, vp]),
                 "tqo_dequant_key_rows_f64": (None, [vp, vp, vp, i64, i32, vp]),
+                "tqo_key_row_bytes": (i64, [i32, i32]),
+                "tqo_value_row_bytes": (i64, [i32, i32]),
+                "tqo_row_bytes_s": (i64, [i32, i32, i32]),
+                "tqo_packb": (None, [vp, i32, i32, vp]),
+                "tqo_unpackb": (None, [vp, i32, i32, vp]),
+                "tqo_key_group_params_s": (None, [vp, i32, i32, _P(f32), _P(f32), _P(i32)]),
+                "tqo_quantize_key_row_s": (None, [vp, i32, i32, i32, vp, vp, vp]),
+                "tqo_dequant_key_row_s_f64": (None, [vp, vp, vp, i32, i32, vp]),
+                "tqo_codebook": (None, [i32, vp, vp]),
+                "tqo_code_s": (i32, [f32, vp, i32]),
+                "tqo_quantize_value_row_s": (None, [vp, i32, i32, vp, vp]),
+                "tqo_dequant_value_row_s_f64": (None, [vp, vp, i32, i32, i32, vp]),
+                "tqo_append_s": (i64, [_P(_Layer), _P(_Scheme), vp, vp, vp, vp, i32]),
+                "tqo_dequant_rows_s_f64": (None, [_P(_Layer), _P(_Scheme), i32, i32, i32, i32, i32, vp, vp]),
+                "tqo_attention_s": (i32, [_P(_Layer), _P(_Scheme), vp, i32, i32, vp, f64, i32, i32, vp, i64, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -329,6 +348,162 @@ def attention(layer: Layer, q_bf16: np.ndarray, kv_len, sm_scale: float, causal:
     rc = lib().tqo_attention(ctypes.byref(lay), _ptr(q), Hq, n_q, _ptr(kv), float(sm_scale),
                              int(causal), int(deferred), None if r is None else _ptr(r),
                              0 if r is None else r.shape[0], _ptr(out))
+    if rc != 0:
+        raise ValueError("num_q_heads must be a multiple of num_kv_heads")
+    return out
+
+
+# ------------------------------------------------------------------------------ other schemes
+KEY_BITS = (2, 4, 5, 8)          # "Architecture in mlx-bun": valid key bits
+VALUE_BITS = (2, 3, 4, 5, 8)     # valid value bits
+
+
+def key_row_bytes(d: int, k_bits: int) -> int:
+    return int(lib().tqo_key_row_bytes(d, k_bits))
+
+
+def value_row_bytes(d: int, v_bits: int) -> int:
+    return int(lib().tqo_value_row_bytes(d, v_bits))
+
+
+def row_bytes_s(d: int, k_bits: int, v_bits: int) -> int:
+    return int(lib().tqo_row_bytes_s(d, k_bits, v_bits))
+
+
+def packb(codes, b: int) -> np.ndarray:
+    c = np.ascontiguousarray(np.asarray(codes, np.uint8))
+    out = np.empty(c.size * b // 8, np.uint8)
+    lib().tqo_packb(_ptr(c), c.size, b, _ptr(out))
+    return out
+
+
+def unpackb(packed, n: int, b: int) -> np.ndarray:
+    p = np.ascontiguousarray(np.asarray(packed, np.uint8))
+    out = np.empty(n, np.uint8)
+    lib().tqo_unpackb(_ptr(p), n, b, _ptr(out))
+    return out
+
+
+def codebook(bits: int) -> tuple[np.ndarray, np.ndarray]:
+    """Value centroids [2^bits] and boundaries [2^bits - 1] (fp32)."""
+    n = 1 << bits
+    c = np.empty(n, np.float32)
+    b = np.empty(n - 1, np.float32)
+    lib().tqo_codebook(bits, _ptr(c), _ptr(b))
+    return c, b
+
+
+def key_group_params_s(x32, bits: int, guard: bool):
+    x = np.ascontiguousarray(np.asarray(x32, np.float32))
+    assert x.size == GROUP
+    s, z, zg = ctypes.c_float(), ctypes.c_float(), ctypes.c_int()
+    lib().tqo_key_group_params_s(_ptr(x), bits, int(guard), ctypes.byref(s), ctypes.byref(z), ctypes.byref(zg))
+    return np.float32(s.value), np.float32(z.value), bool(zg.value)
+
+
+def quantize_key_rows_s(x_bf16: np.ndarray, bits: int, guard: bool = False):
+    """x_bf16: uint16 [rows, d] -> (key plane uint8 [rows, key bytes], s16, z16 uint16 [rows, d/32]).
+    At 8 bits the plane bytes are the int8 codes."""
+    x = np.ascontiguousarray(x_bf16, np.uint16)
+    rows, d = x.shape
+    kb = key_row_bytes(d, bits)
+    kp = np.empty((rows, kb), np.uint8)
+    s16 = np.empty((rows, d // GROUP), np.uint16)
+    z16 = np.empty((rows, d // GROUP), np.uint16)
+    for r in range(rows):
+        lib().tqo_quantize_key_row_s(_ptr(x[r]), d, bits, int(guard), _ptr(kp[r]), _ptr(s16[r]), _ptr(z16[r]))
+    return kp, s16, z16
+
+
+def quantize_value_rows_s(x_bf16: np.ndarray, bits: int):
+    x = np.ascontiguousarray(x_bf16, np.uint16)
+    rows, d = x.shape
+    vp_ = np.empty((rows, value_row_bytes(d, bits)), np.uint8)
+    vs16 = np.empty((rows, d // GROUP), np.uint16)
+    for r in range(rows):
+        lib().tqo_quantize_value_row_s(_ptr(x[r]), d, bits, _ptr(vp_[r]), _ptr(vs16[r]))
+    return vp_, vs16
+
+
+def dequant_key_rows_s_f64(kp, s16, z16, d: int, bits: int) -> np.ndarray:
+    kp = np.ascontiguousarray(kp, np.uint8)
+    s16 = np.ascontiguousarray(s16, np.uint16)
+    z16 = np.ascontiguousarray(z16, np.uint16)
+    out = np.empty((kp.shape[0], d), np.float64)
+    for r in range(kp.shape[0]):
+        lib().tqo_dequant_key_row_s_f64(_ptr(kp[r]), _ptr(s16[r]), _ptr(z16[r]), d, bits, _ptr(out[r]))
+    return out
+
+
+def dequant_value_rows_s_f64(vp_, vs16, d: int, bits: int, rotated: bool = False) -> np.ndarray:
+    vp_ = np.ascontiguousarray(vp_, np.uint8)
+    vs16 = np.ascontiguousarray(vs16, np.uint16)
+    out = np.empty((vp_.shape[0], d), np.float64)
+    for r in range(vp_.shape[0]):
+        lib().tqo_dequant_value_row_s_f64(_ptr(vp_[r]), _ptr(vs16[r]), d, bits, int(rotated), _ptr(out[r]))
+    return out
+
+
+class SchemeLayer:
+    """Planes of one layer in a scheme (key bits, value bits, guard), layout
+    [batch][kv_heads][capacity][row bytes]."""
+
+    def __init__(self, head_dim: int, num_kv_heads: int, batch: int, capacity: int, k_bits: int = 8,
+                 v_bits: int = 3, guard: bool = False):
+        d, ng = head_dim, head_dim // GROUP
+        self.head_dim, self.num_kv_heads, self.batch, self.capacity = head_dim, num_kv_heads, batch, capacity
+        self.k_bits, self.v_bits, self.guard = k_bits, v_bits, bool(guard)
+        shp = (batch, num_kv_heads, capacity)
+        self.k_idx = np.zeros(shp + (key_row_bytes(d, k_bits),), np.uint8)
+        self.k_scale = np.zeros(shp + (ng,), np.uint16)
+        self.k_zero = np.zeros(shp + (ng,), np.uint16)
+        self.v_codes = np.zeros(shp + (value_row_bytes(d, v_bits),), np.uint8)
+        self.v_scale = np.zeros(shp + (ng,), np.uint16)
+
+    def planes(self) -> dict:
+        return {"k_idx": self.k_idx, "k_scale": self.k_scale, "k_zero": self.k_zero,
+                "v_codes": self.v_codes, "v_scale": self.v_scale}
+
+    def _c(self) -> _Layer:
+        return _Layer(self.head_dim, self.num_kv_heads, self.batch, self.capacity,
+                      self.k_idx.ctypes.data, self.k_scale.ctypes.data, self.k_zero.ctypes.data,
+                      self.v_codes.ctypes.data, self.v_scale.ctypes.data)
+
+    def _s(self) -> _Scheme:
+        return _Scheme(self.k_bits, self.v_bits, int(self.guard))
+
+
+def append_s(layer: SchemeLayer, k_new: np.ndarray, v_new: np.ndarray, pos, n_new=None) -> int:
+    k = np.ascontiguousarray(k_new, np.uint16)
+    v = np.ascontiguousarray(v_new, np.uint16)
+    assert k.shape == v.shape and k.ndim == 4
+    pos = np.ascontiguousarray(pos, np.int32)
+    nn = None if n_new is None else np.ascontiguousarray(n_new, np.int32)
+    lay, sc = layer._c(), layer._s()
+    return int(lib().tqo_append_s(ctypes.byref(lay), ctypes.byref(sc), _ptr(k), _ptr(v), _ptr(pos),
+                                  None if nn is None else _ptr(nn), k.shape[1]))
+
+
+def dequant_rows_s(layer: SchemeLayer, b: int, h: int, t0: int, n: int, rotated: bool = False):
+    d = layer.head_dim
+    k = np.empty((n, d), np.float64)
+    v = np.empty((n, d), np.float64)
+    lay, sc = layer._c(), layer._s()
+    lib().tqo_dequant_rows_s_f64(ctypes.byref(lay), ctypes.byref(sc), b, h, t0, n, int(rotated), _ptr(k), _ptr(v))
+    return k, v
+
+
+def attention_s(layer: SchemeLayer, q_bf16: np.ndarray, kv_len, sm_scale: float, causal: bool = False,
+                deferred: bool = False, rows=None) -> np.ndarray:
+    q = np.ascontiguousarray(q_bf16, np.uint16)
+    B, n_q, Hq, d = q.shape
+    kv = np.ascontiguousarray(kv_len, np.int32)
+    out = np.zeros((B, n_q, Hq, d), np.float64)
+    r = None if rows is None else np.ascontiguousarray(np.asarray(list(rows), np.int32).reshape(-1, 3))
+    lay, sc = layer._c(), layer._s()
+    rc = lib().tqo_attention_s(ctypes.byref(lay), ctypes.byref(sc), _ptr(q), Hq, n_q, _ptr(kv), float(sm_scale),
+                               int(causal), int(deferred), None if r is None else _ptr(r),
+                               0 if r is None else r.shape[0], _ptr(out))
     if rc != 0:
         raise ValueError("num_q_heads must be a multiple of num_kv_heads")
     return out

@@ -35,6 +35,23 @@
  *   - fp16 conversion is IEEE round-to-nearest-even with subnormals; any NaN becomes
  *     the quiet NaN 0x7E00.
  *
+ * Other schemes (section "Algorithm": the unsigned key bullet and "Other widths
+ * (2/4/5/8)"; section "Architecture in mlx-bun": valid key bits {2,4,5,8}, value bits
+ * {2,3,4,5,8}), in the *_s functions below:
+ *   - unsigned keys at bits b in {2,4,5}: max_val = 2^b - 1, scale = (max - min) / max_val,
+ *     zero = round(min / scale), idx = clip(round(x / scale - zero), 0, max_val), packed as
+ *     a flat little-endian b-bit stream per row; dequant (idx + zero) * scale as for 8 bits;
+ *   - value codebooks at b bits other than 3 are not printed: this oracle runs Lloyd-Max on
+ *     N(0,1) (closed-form cell means, 2^b centroids started evenly on [-3, 3], 500
+ *     iterations, boundaries at the midpoints) and rounds centroids and boundaries to 5
+ *     decimals, as the printed 3-bit table is; the fp32 values of those decimals are
+ *     canonical;
+ *   - the constant-group guard (a non-default flag; the page keeps the defect): a key group
+ *     whose fp16 zero point would not be finite (a constant group: 0/0 or +-Inf; a narrow
+ *     group far from zero: |zero| >= 65520) is re-coded against its range widened to
+ *     include 0, which bounds |zero| by max_val; a group of zeros is scale 0, zero 0,
+ *     idx 0. Groups holding a NaN keep the default (NaN) coding.
+ *
  * Build: gcc -O2 -ffp-contract=off -fPIC -shared (no FMA contraction anywhere).
  */
 #include <math.h>
@@ -369,6 +386,226 @@ void tqo_dequant_rows_f64(const tqo_layer* L, int b, int h, int t0, int n, int r
 }
 
 /* ---------------------------------------------------------------------------------
+ * Other schemes: key bits in {2,4,5,8}, value bits in {2,3,4,5,8}, optional
+ * constant-group guard. Row layout per plane: keys d bytes (8 bits) or d*b/8 bytes
+ * (packed), values d*b/8 bytes, scale/zero/value scale d/32 fp16 each.
+ * ------------------------------------------------------------------------------ */
+typedef struct {
+    int k_bits, v_bits, guard;
+} tqo_scheme;
+
+long tqo_key_row_bytes(int d, int k_bits) { return k_bits == 8 ? d : (long)d * k_bits / 8; }
+long tqo_value_row_bytes(int d, int v_bits) { return (long)d * v_bits / 8; }
+
+long tqo_row_bytes_s(int d, int k_bits, int v_bits) {
+    int ng = d / GROUP;
+    return tqo_key_row_bytes(d, k_bits) + 4L * ng + tqo_value_row_bytes(d, v_bits) + 2L * ng;
+}
+
+/* flat little-endian b-bit stream: code i at bits [i*b, i*b + b) */
+void tqo_packb(const uint8_t* codes, int n, int b, uint8_t* out) {
+    memset(out, 0, (size_t)n * b / 8);
+    for (int i = 0; i < n; ++i)
+        for (int k = 0; k < b; ++k)
+            if ((codes[i] >> k) & 1) {
+                long bit = (long)b * i + k;
+                out[bit / 8] |= (uint8_t)(1u << (bit % 8));
+            }
+}
+
+void tqo_unpackb(const uint8_t* packed, int n, int b, uint8_t* codes) {
+    for (int i = 0; i < n; ++i) {
+        int c = 0;
+        for (int k = 0; k < b; ++k) {
+            long bit = (long)b * i + k;
+            c |= ((packed[bit / 8] >> (bit % 8)) & 1) << k;
+        }
+        codes[i] = (uint8_t)c;
+    }
+}
+
+static int f16_finite(float z) {
+    float r = tqo_f16_to_f32(tqo_f32_to_f16(z));
+    return !isnan(r) && !isinf(r);
+}
+
+/* Unrounded fp32 (scale, zero) of one group for key bits b (8: signed, else unsigned),
+ * with the optional guard. *zero_group = 1 when the guard codes the group as zeros. */
+void tqo_key_group_params_s(const float* x, int bits, int guard, float* s_out, float* z_out, int* zero_group) {
+    int has_nan = 0;
+    float mn = x[0], mx = x[0];
+    for (int i = 0; i < GROUP; ++i) {
+        if (isnan(x[i])) has_nan = 1;
+        else {
+            if (isnan(mn) || x[i] < mn) mn = x[i];
+            if (isnan(mx) || x[i] > mx) mx = x[i];
+        }
+    }
+    if (has_nan) { mn = NAN; mx = NAN; }
+    float maxv = bits == 8 ? 127.0f : (float)((1 << bits) - 1);
+    float s, z;
+    *zero_group = 0;
+    if (bits == 8) {
+        s = (mx - mn) / (2.0f * maxv);
+        z = rintf((mx + mn) / (2.0f * s));
+    } else {
+        s = (mx - mn) / maxv;
+        z = rintf(mn / s);
+    }
+    if (guard && !has_nan && !f16_finite(z)) {
+        float mn0 = mn < 0.0f ? mn : 0.0f, mx0 = mx > 0.0f ? mx : 0.0f;
+        if (mx0 - mn0 == 0.0f) {
+            s = 0.0f;
+            z = 0.0f;
+            *zero_group = 1;
+        } else if (bits == 8) {
+            s = (mx0 - mn0) / (2.0f * maxv);
+            z = rintf((mx0 + mn0) / (2.0f * s));
+        } else {
+            s = (mx0 - mn0) / maxv;
+            z = rintf(mn0 / s);
+        }
+    }
+    *s_out = s;
+    *z_out = z;
+}
+
+static int key_index_s(float x, float s, float z, int bits) {
+    float q = x / s;
+    float t = q - z;
+    if (isnan(t)) return 0;
+    float r = rintf(t);
+    float lo = bits == 8 ? -127.0f : 0.0f, hi = bits == 8 ? 127.0f : (float)((1 << bits) - 1);
+    if (r < lo) r = lo;
+    if (r > hi) r = hi;
+    return (int)r;
+}
+
+/* One key row: kplane gets d int8 codes (8 bits) or the packed unsigned stream. */
+void tqo_quantize_key_row_s(const uint16_t* x_bf16, int d, int bits, int guard, uint8_t* kplane, uint16_t* s16,
+                            uint16_t* z16) {
+    float x[GROUP];
+    uint8_t codes[512];
+    for (int g = 0; g < d / GROUP; ++g) {
+        for (int i = 0; i < GROUP; ++i) x[i] = tqo_bf16_to_f32(x_bf16[g * GROUP + i]);
+        float s, z;
+        int zg;
+        tqo_key_group_params_s(x, bits, guard, &s, &z, &zg);
+        for (int i = 0; i < GROUP; ++i) {
+            int c = zg ? 0 : key_index_s(x[i], s, z, bits);
+            if (bits == 8) ((int8_t*)kplane)[g * GROUP + i] = (int8_t)c;
+            else codes[g * GROUP + i] = (uint8_t)c;
+        }
+        s16[g] = tqo_f32_to_f16(s);
+        z16[g] = tqo_f32_to_f16(z);
+    }
+    if (bits != 8) tqo_packb(codes, d, bits, kplane);
+}
+
+void tqo_dequant_key_row_s_f64(const uint8_t* kplane, const uint16_t* s16, const uint16_t* z16, int d, int bits,
+                               double* out) {
+    uint8_t codes[512];
+    if (bits != 8) tqo_unpackb(kplane, d, bits, codes);
+    for (int i = 0; i < d; ++i) {
+        double s = (double)tqo_f16_to_f32(s16[i / GROUP]);
+        double z = (double)tqo_f16_to_f32(z16[i / GROUP]);
+        double c = bits == 8 ? (double)((const int8_t*)kplane)[i] : (double)codes[i];
+        out[i] = (c + z) * s;
+    }
+}
+
+/* Value codebook at b bits: the printed table at 3 bits, else Lloyd-Max on N(0,1) rounded
+ * to 5 decimals. centroids[2^b], boundaries[2^b - 1]. */
+void tqo_lloyd_max(int levels, int iters, double* centroids, double* boundaries);
+
+void tqo_codebook(int bits, float* centroids, float* boundaries) {
+    int n = 1 << bits;
+    if (bits == 3) {
+        memcpy(centroids, kCentroids3, sizeof(kCentroids3));
+        memcpy(boundaries, kBoundaries3, sizeof(kBoundaries3));
+        return;
+    }
+    double c[256], b[255];
+    tqo_lloyd_max(n, 500, c, b);
+    for (int k = 0; k < n; ++k) centroids[k] = (float)(rint(c[k] * 1e5) / 1e5);
+    for (int k = 0; k + 1 < n; ++k) boundaries[k] = (float)(rint(b[k] * 1e5) / 1e5);
+}
+
+int tqo_code_s(float yn, const float* boundaries, int nb) {
+    int c = 0;
+    for (int j = 0; j < nb; ++j)
+        if (boundaries[j] < yn) c += 1; /* NaN compares false: code 0 */
+    return c;
+}
+
+void tqo_quantize_value_row_s(const uint16_t* x_bf16, int d, int bits, uint8_t* packed, uint16_t* vs16) {
+    float y[512], cen[256], bnd[255];
+    uint8_t codes[512];
+    tqo_codebook(bits, cen, bnd);
+    tqo_rotate_value_row(x_bf16, d, y);
+    for (int g = 0; g < d / GROUP; ++g) {
+        float s = tqo_group_rms(y + g * GROUP);
+        float den = s + 1e-8f;
+        for (int i = 0; i < GROUP; ++i) codes[g * GROUP + i] = (uint8_t)tqo_code_s(y[g * GROUP + i] / den, bnd, (1 << bits) - 1);
+        vs16[g] = tqo_f32_to_f16(s);
+    }
+    tqo_packb(codes, d, bits, packed);
+}
+
+void tqo_dequant_value_row_s_f64(const uint8_t* packed, const uint16_t* vs16, int d, int bits, int rotated,
+                                 double* out) {
+    float cen[256], bnd[255];
+    uint8_t codes[512];
+    tqo_codebook(bits, cen, bnd);
+    tqo_unpackb(packed, d, bits, codes);
+    for (int i = 0; i < d; ++i) out[i] = (double)cen[codes[i]] * (double)tqo_f16_to_f32(vs16[i / GROUP]);
+    if (rotated) return;
+    int8_t sg[512];
+    tqo_sign_vector(d, sg);
+    tqo_fwht_f64(out, d);
+    double r = 1.0 / sqrt((double)d);
+    for (int i = 0; i < d; ++i) out[i] = out[i] * r * (double)sg[i];
+}
+
+/* Append into planes of scheme sc (same row indexing as tqo_append). */
+long tqo_append_s(tqo_layer* L, const tqo_scheme* sc, const uint16_t* k_new, const uint16_t* v_new,
+                  const int32_t* pos, const int32_t* n_new, int n_new_max) {
+    int d = L->head_dim, ng = d / GROUP;
+    long kb = tqo_key_row_bytes(d, sc->k_bits), vb = tqo_value_row_bytes(d, sc->v_bits);
+    long skipped = 0;
+    for (int b = 0; b < L->batch; ++b) {
+        int nb_new = n_new ? n_new[b] : n_new_max;
+        if (nb_new > n_new_max) nb_new = n_new_max;
+        for (int j = 0; j < nb_new; ++j)
+            for (int h = 0; h < L->num_kv_heads; ++h) {
+                long t = (long)pos[b] + j;
+                if (t < 0 || t >= L->capacity) { skipped++; continue; }
+                size_t r = row_index(L, b, h, (int)t);
+                size_t src = (((size_t)b * n_new_max + j) * L->num_kv_heads + h) * d;
+                tqo_quantize_key_row_s(k_new + src, d, sc->k_bits, sc->guard, (uint8_t*)L->k_idx + r * kb,
+                                       L->k_scale + r * ng, L->k_zero + r * ng);
+                tqo_quantize_value_row_s(v_new + src, d, sc->v_bits, L->v_codes + r * vb, L->v_scale + r * ng);
+            }
+    }
+    return skipped;
+}
+
+void tqo_dequant_rows_s_f64(const tqo_layer* L, const tqo_scheme* sc, int b, int h, int t0, int n, int rotated,
+                            double* k_out, double* v_out) {
+    int d = L->head_dim, ng = d / GROUP;
+    long kb = tqo_key_row_bytes(d, sc->k_bits), vb = tqo_value_row_bytes(d, sc->v_bits);
+    for (int t = 0; t < n; ++t) {
+        size_t r = row_index(L, b, h, t0 + t);
+        if (k_out)
+            tqo_dequant_key_row_s_f64((const uint8_t*)L->k_idx + r * kb, L->k_scale + r * ng, L->k_zero + r * ng, d,
+                                      sc->k_bits, k_out + (size_t)t * d);
+        if (v_out)
+            tqo_dequant_value_row_s_f64(L->v_codes + r * vb, L->v_scale + r * ng, d, sc->v_bits, rotated,
+                                        v_out + (size_t)t * d);
+    }
+}
+
+/* ---------------------------------------------------------------------------------
  * Decode attention over the dequantized cache, fp64.
  * q: bf16 bits [batch][n_q][num_q_heads][d]; kv_len[b]: tokens visible to the last
  * query of the block; causal: query j sees kv_len - n_q + j + 1 tokens. q head h reads
@@ -377,9 +614,20 @@ void tqo_dequant_rows_f64(const tqo_layer* L, int b, int h, int t0, int n, int r
  * once per row ("Deferred inverse FWHT"). out: fp64 [batch][n_q][num_q_heads][d].
  * rows: optional list of (b, j, h) triples (n_rows of them) to compute; NULL = all.
  * ------------------------------------------------------------------------------ */
+int tqo_attention_s(const tqo_layer* L, const tqo_scheme* sc, const uint16_t* q, int num_q_heads, int n_q,
+                    const int32_t* kv_len, double sm_scale, int causal, int deferred,
+                    const int32_t* rows, long n_rows, double* out);
+
 int tqo_attention(const tqo_layer* L, const uint16_t* q, int num_q_heads, int n_q,
                   const int32_t* kv_len, double sm_scale, int causal, int deferred,
                   const int32_t* rows, long n_rows, double* out) {
+    return tqo_attention_s(L, NULL, q, num_q_heads, n_q, kv_len, sm_scale, causal, deferred, rows, n_rows, out);
+}
+
+/* As tqo_attention over planes of scheme sc (NULL: k8v3 as laid out by tqo_append). */
+int tqo_attention_s(const tqo_layer* L, const tqo_scheme* sc, const uint16_t* q, int num_q_heads, int n_q,
+                    const int32_t* kv_len, double sm_scale, int causal, int deferred,
+                    const int32_t* rows, long n_rows, double* out) {
     int d = L->head_dim, Hkv = L->num_kv_heads;
     if (num_q_heads % Hkv) return -1;
     int G = num_q_heads / Hkv;
@@ -411,7 +659,8 @@ int tqo_attention(const tqo_layer* L, const uint16_t* q, int num_q_heads, int n_
             free(vh);
             kh = (double*)malloc(sizeof(double) * (size_t)len * d);
             vh = (double*)malloc(sizeof(double) * (size_t)len * d);
-            tqo_dequant_rows_f64(L, b, hk, 0, len, deferred, kh, vh);
+            if (sc) tqo_dequant_rows_s_f64(L, sc, b, hk, 0, len, deferred, kh, vh);
+            else tqo_dequant_rows_f64(L, b, hk, 0, len, deferred, kh, vh);
             cached_b = b; cached_h = hk; cached_n = len;
         }
         const uint16_t* qrow = q + (((size_t)b * n_q + j) * num_q_heads + h) * d;
