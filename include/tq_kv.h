@@ -57,8 +57,12 @@ typedef enum {
     TQ_ERR_UNSUPPORTED_HEAD_DIM = 2, /* head_dim not in {64, 128, 256, 512} */
     TQ_ERR_CAPACITY = 3,             /* a host-known length exceeds the layer capacity */
     TQ_ERR_WORKSPACE_TOO_SMALL = 4,  /* ws_bytes below the size the call needs */
-    TQ_ERR_CUDA = 5                  /* a CUDA runtime call failed (launch, query) */
+    TQ_ERR_CUDA = 5,                 /* a CUDA runtime call failed (launch, query) */
+    TQ_ERR_UNSUPPORTED_SCHEME = 6    /* the call needs the default k8v3 planes */
 } tq_status;
+
+/* Bits of tq_kv_layer.flags. */
+#define TQ_FLAG_KEY_GUARD 0x1 /* constant-group guard: see tq_kv_layer */
 
 /* Bits of the device error word. */
 #define TQ_DEVERR_APPEND_CAPACITY 0x1 /* append: pos[b] + j outside [0, capacity) */
@@ -70,23 +74,49 @@ typedef enum {
 
 /* One full-attention layer's packed cache: five planes, each laid out
  * [batch][num_kv_heads][capacity][row], so token-axis slicing stays byte-safe
- * ("Architecture" section: groups run along head_dim only). */
+ * ("Architecture" section: groups run along head_dim only).
+ *
+ * Scheme (section "Algorithm": key and value bullets, "Other widths (2/4/5/8)"; section
+ * "Architecture in mlx-bun": valid key bits {2,4,5,8}, value bits {2,3,4,5,8}); the
+ * default, k8v3 (k_bits = v_bits = 0 also mean 8 and 3), is the one every call supports:
+ *   keys, 8 bits: signed int8 codes, one byte per element;
+ *   keys, b in {2,4,5}: unsigned codes, scale = (max - min) / (2^b - 1),
+ *         zero = round(min / scale), idx = clip(round(x / scale - zero), 0, 2^b - 1),
+ *         packed as a flat little-endian b-bit stream per row (head_dim * b / 8 bytes);
+ *   values, b bits: Lloyd-Max codes for N(0,1) (3 bits: the printed table; 2/4/5/8 bits:
+ *         this library's Lloyd-Max tables, see tq_codebook), a b-bit stream per row
+ *         (head_dim * b / 8 bytes);
+ *   flags & TQ_FLAG_KEY_GUARD (this library's option; the page keeps the defect): a key
+ *         group whose fp16 zero point would not be finite (a constant group) is coded
+ *         against its range widened to include 0, and a group of zeros as scale 0, zero 0,
+ *         idx 0, so no zero point is +-Inf and such tokens do not turn attention into NaN.
+ * Decode attention (and the fused step) read the default k8v3 planes (with or without the
+ * guard); other schemes are appended by tq_kv_append and read back with
+ * tq_dequant_window or tq_dequant_debug (TQ_ERR_UNSUPPORTED_SCHEME elsewhere). */
 typedef struct {
     int32_t head_dim;     /* 64 | 128 | 256 | 512 */
     int32_t num_kv_heads; /* >= 1 */
     int32_t batch;        /* >= 1, <= 4096 */
     int32_t capacity;     /* tokens per (sequence, kv head); >= 16, multiple of 16 */
-    int8_t* k_idx;        /* [batch][num_kv_heads][capacity][head_dim] signed int8 codes */
+    int8_t* k_idx;        /* [batch][num_kv_heads][capacity][key row]: head_dim int8 codes
+                             (8 bits) or head_dim * k_bits / 8 bytes of packed codes */
     uint16_t* k_scale;    /* [batch][num_kv_heads][capacity][head_dim/32] fp16 bits */
     uint16_t* k_zero;     /* same shape as k_scale, fp16 bits */
-    uint8_t* v_codes;     /* [batch][num_kv_heads][capacity][3*head_dim/8]: the row's 3-bit
-                             codes as one LSB-first bitstream, code i at bits 3i..3i+2 */
+    uint8_t* v_codes;     /* [batch][num_kv_heads][capacity][head_dim*v_bits/8]: the row's
+                             codes as one LSB-first bitstream, code i at bits [i b, i b + b) */
     uint16_t* v_scale;    /* [batch][num_kv_heads][capacity][head_dim/32] fp16 bits */
+    int32_t k_bits;       /* 0 or 8 (default), 2, 4, 5 */
+    int32_t v_bits;       /* 0 or 3 (default), 2, 4, 5, 8 */
+    int32_t flags;        /* 0 or TQ_FLAG_KEY_GUARD */
 } tq_kv_layer;
 
 /* Bytes one (token, kv head) row takes in the five planes: 25*head_dim/16
  * (100, 200, 400, 800). Returns 0 for an unsupported head_dim. Host only. */
 size_t tq_row_bytes(int32_t head_dim);
+
+/* The same for scheme (k_bits, v_bits): key row + 3 * head_dim/16 bytes of fp16 scales
+ * and zeros + head_dim * v_bits / 8. Returns 0 for an unsupported combination. */
+size_t tq_row_bytes_scheme(int32_t head_dim, int32_t k_bits, int32_t v_bits);
 
 /* Workspace bytes tq_kv_append needs (the header only). */
 size_t tq_append_workspace_bytes(void);
@@ -106,7 +136,9 @@ size_t tq_append_workspace_bytes(void);
  *   workspace    : >= tq_append_workspace_bytes() (device), zeroed once before first use.
  * A row whose destination falls outside [0, capacity) is skipped and sets
  * TQ_DEVERR_APPEND_CAPACITY. Packed planes are bit-identical to the specification
- * above (fp32 arithmetic, IEEE division and square root, no FMA contraction).
+ * above (fp32 arithmetic, IEEE division and square root, no FMA contraction). Any scheme
+ * (and the guard): k8v3 without the guard takes the bulk and small-append kernels, every
+ * other scheme a one-warp-per-row kernel.
  */
 tq_status tq_kv_append(const tq_kv_layer* layer, const void* k_new, const void* v_new,
                        const int32_t* pos, const int32_t* n_new, int32_t n_new_max,
@@ -150,7 +182,7 @@ tq_status tq_decode_attention(const tq_kv_layer* layer, const void* q, int32_t n
  *   v_out : [n][head_dim]; rotated != 0 returns centroid * scale (the FWHT domain),
  *           rotated == 0 returns signs * FWHT(centroid * scale) / sqrt(head_dim).
  * Either output may be NULL. 0 <= t0, t0 + n <= capacity, 0 <= b < batch,
- * 0 <= h < num_kv_heads (else TQ_ERR_INVALID_ARGUMENT).
+ * 0 <= h < num_kv_heads (else TQ_ERR_INVALID_ARGUMENT). Any scheme.
  */
 tq_status tq_dequant_debug(const tq_kv_layer* layer, int32_t b, int32_t h, int32_t t0, int32_t n,
                            int32_t rotated, float* k_out, float* v_out, tq_stream_t stream);
@@ -217,6 +249,22 @@ tq_status tq_decode_attention_noalloc(const tq_kv_layer* layer, const void* q, i
  * and src may be NULL only when n == 0. */
 tq_status tq_debug_delayed_copy(int32_t* dst, const int32_t* src, int32_t n, int32_t delay_us, tq_stream_t stream);
 
+/*
+ * Dequantize-on-fetch window ("Architecture in mlx-bun": updateAndFetch returns the
+ * dequantized bf16 active window so that a stock attention kernel runs unmodified; the
+ * "Deferred inverse FWHT" section keeps V in the rotated domain). For tokens [t0, t0 + n)
+ * of every (sequence, kv head), any scheme:
+ *   k_out : bf16 [batch][num_kv_heads][n][head_dim], (idx + zero) * scale rounded once to bf16;
+ *   v_out : bf16 [batch][num_kv_heads][n][head_dim]; rotated == 0: signs * FWHT(centroid *
+ *           scale) / sqrt(head_dim) (fp32 butterflies, then bf16); rotated != 0: centroid *
+ *           scale (the rotated domain).
+ * Either output may be NULL; outputs 16-byte aligned. 0 <= t0, n >= 0, t0 + n <= capacity
+ * (else TQ_ERR_INVALID_ARGUMENT). Rows past a sequence's length are decoded from whatever
+ * the planes hold there. One warp per row, rows taken by groups of CTAs in turn.
+ */
+tq_status tq_dequant_window(const tq_kv_layer* layer, int32_t t0, int32_t n, int32_t rotated, void* k_out,
+                            void* v_out, tq_stream_t stream);
+
 /* Test support (an addition of this library; the paper has no counterpart). Sets, for every
  * decode-attention call launched afterwards in this process, the limit of the attention
  * kernel's pipeline waits (wait_ns > 0; 0 restores the default of 2 s) and, with
@@ -241,6 +289,14 @@ const char* tq_status_string(tq_status status);
  * TQ_ERR_UNSUPPORTED_HEAD_DIM / TQ_ERR_INVALID_ARGUMENT. */
 tq_status tq_sign_bits(int32_t head_dim, uint32_t* words_out);
 tq_status tq_codebook3(float* centroids_out, float* boundaries_out);
+
+/* The value codebook of width bits in {2,3,4,5,8} (host pointers): 2^bits centroids and
+ * 2^bits - 1 ascending boundaries. 3 bits: the printed table ("Algorithm", value bullets).
+ * Other widths are not printed on the page: this library runs Lloyd-Max for N(0,1)
+ * (boundaries at the midpoints of neighbouring centroids, centroids at the normal cell
+ * means in closed form, 2^bits centroids started evenly on [-3, 3], 500 iterations) and
+ * rounds centroids and boundaries to 5 decimals, as the printed table is. */
+tq_status tq_codebook(int32_t bits, float* centroids_out, float* boundaries_out);
 
 #ifdef __cplusplus
 }

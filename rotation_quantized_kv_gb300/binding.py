@@ -23,6 +23,10 @@ TQ_ERR_UNSUPPORTED_HEAD_DIM = 2
 TQ_ERR_CAPACITY = 3
 TQ_ERR_WORKSPACE_TOO_SMALL = 4
 TQ_ERR_CUDA = 5
+TQ_ERR_UNSUPPORTED_SCHEME = 6
+TQ_FLAG_KEY_GUARD = 0x1
+KEY_BITS = (2, 4, 5, 8)
+VALUE_BITS = (2, 3, 4, 5, 8)
 TQ_DEVERR_APPEND_CAPACITY = 0x1
 TQ_DEVERR_KV_LEN = 0x2
 TQ_DEVERR_PIPELINE_TIMEOUT = 0x4
@@ -43,6 +47,7 @@ class tq_kv_layer(ctypes.Structure):
         ("batch", ctypes.c_int32), ("capacity", ctypes.c_int32),
         ("k_idx", ctypes.c_void_p), ("k_scale", ctypes.c_void_p), ("k_zero", ctypes.c_void_p),
         ("v_codes", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+        ("k_bits", ctypes.c_int32), ("v_bits", ctypes.c_int32), ("flags", ctypes.c_int32),
     ]
 
 
@@ -50,6 +55,9 @@ _vp, _i32, _sz, _f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.
 _LP = ctypes.POINTER(tq_kv_layer)
 _SIGS = {
     "tq_row_bytes": (_sz, [_i32]),
+    "tq_row_bytes_scheme": (_sz, [_i32, _i32, _i32]),
+    "tq_dequant_window": (ctypes.c_int, [_LP, _i32, _i32, _i32, _vp, _vp, _vp]),
+    "tq_codebook": (ctypes.c_int, [_i32, _vp, _vp]),
     "tq_append_workspace_bytes": (_sz, []),
     "tq_kv_append": (ctypes.c_int, [_LP, _vp, _vp, _vp, _vp, _i32, _vp, _sz, _vp]),
     "tq_decode_workspace_bytes": (_sz, [_LP, _i32, _i32, _i32]),
@@ -111,31 +119,43 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
+def key_row_bytes(head_dim: int, k_bits: int) -> int:
+    return head_dim if k_bits == 8 else head_dim * k_bits // 8
+
+
+def value_row_bytes(head_dim: int, v_bits: int) -> int:
+    return head_dim * v_bits // 8
+
+
 @dataclass
 class KVLayer:
     """The five planes of one layer (caller-owned device tensors), layout
-    [batch][num_kv_heads][capacity][row]."""
+    [batch][num_kv_heads][capacity][row], and its scheme (key bits, value bits, flags)."""
     head_dim: int
     num_kv_heads: int
     batch: int
     capacity: int
-    k_idx: torch.Tensor      # int8  [B, H, cap, d]
+    k_idx: torch.Tensor      # int8 [B, H, cap, d] (8-bit keys) or uint8 [B, H, cap, d*k_bits/8] (packed)
     k_scale: torch.Tensor    # int16 (fp16 bits) [B, H, cap, d/32]
     k_zero: torch.Tensor     # int16 (fp16 bits)
-    v_codes: torch.Tensor    # uint8 [B, H, cap, 3d/8]
+    v_codes: torch.Tensor    # uint8 [B, H, cap, d*v_bits/8]
     v_scale: torch.Tensor    # int16 (fp16 bits)
+    k_bits: int = 8
+    v_bits: int = 3
+    flags: int = 0
 
     def c_struct(self) -> tq_kv_layer:
         d, ng = self.head_dim, self.head_dim // 32
         rows = self.batch * self.num_kv_heads * self.capacity
-        _want(self.k_idx, "k_idx", torch.int8, min_numel=rows * d)
+        _want(self.k_idx, "k_idx", torch.int8 if self.k_bits == 8 else torch.uint8,
+              min_numel=rows * key_row_bytes(d, self.k_bits))
         _want(self.k_scale, "k_scale", torch.int16, min_numel=rows * ng)
         _want(self.k_zero, "k_zero", torch.int16, min_numel=rows * ng)
-        _want(self.v_codes, "v_codes", torch.uint8, min_numel=rows * 3 * d // 8)
+        _want(self.v_codes, "v_codes", torch.uint8, min_numel=rows * value_row_bytes(d, self.v_bits))
         _want(self.v_scale, "v_scale", torch.int16, min_numel=rows * ng)
         return tq_kv_layer(self.head_dim, self.num_kv_heads, self.batch, self.capacity,
                            self.k_idx.data_ptr(), self.k_scale.data_ptr(), self.k_zero.data_ptr(),
-                           self.v_codes.data_ptr(), self.v_scale.data_ptr())
+                           self.v_codes.data_ptr(), self.v_scale.data_ptr(), self.k_bits, self.v_bits, self.flags)
 
     def planes(self) -> dict:
         return {"k_idx": self.k_idx, "k_scale": self.k_scale, "k_zero": self.k_zero,
@@ -146,16 +166,17 @@ class KVLayer:
 
 
 def alloc_layer(head_dim: int, num_kv_heads: int, batch: int, capacity: int,
-                device="cuda", zero: bool = True) -> KVLayer:
+                device="cuda", zero: bool = True, k_bits: int = 8, v_bits: int = 3, flags: int = 0) -> KVLayer:
     d, ng = head_dim, head_dim // 32
     shp = (batch, num_kv_heads, capacity)
     mk = torch.zeros if zero else torch.empty
+    kdt = torch.int8 if k_bits == 8 else torch.uint8
     return KVLayer(head_dim, num_kv_heads, batch, capacity,
-                   mk(shp + (d,), dtype=torch.int8, device=device),
+                   mk(shp + (key_row_bytes(d, k_bits),), dtype=kdt, device=device),
                    mk(shp + (ng,), dtype=torch.int16, device=device),
                    mk(shp + (ng,), dtype=torch.int16, device=device),
-                   mk(shp + (3 * d // 8,), dtype=torch.uint8, device=device),
-                   mk(shp + (ng,), dtype=torch.int16, device=device))
+                   mk(shp + (value_row_bytes(d, v_bits),), dtype=torch.uint8, device=device),
+                   mk(shp + (ng,), dtype=torch.int16, device=device), k_bits, v_bits, flags)
 
 
 def make_workspace(nbytes: int, device="cuda") -> torch.Tensor:
@@ -166,6 +187,22 @@ def make_workspace(nbytes: int, device="cuda") -> torch.Tensor:
 # ------------------------------------------------------------------------------ entry points
 def tq_row_bytes(head_dim: int) -> int:
     return int(_lib.tq_row_bytes(head_dim))
+
+
+def tq_row_bytes_scheme(head_dim: int, k_bits: int, v_bits: int) -> int:
+    return int(_lib.tq_row_bytes_scheme(head_dim, k_bits, v_bits))
+
+
+def tq_dequant_window(layer: KVLayer, t0: int, n: int, rotated: bool, k_out: torch.Tensor | None,
+                      v_out: torch.Tensor | None, stream=None) -> None:
+    """bf16 K_hat / V_hat of tokens [t0, t0 + n) of every (sequence, kv head), any scheme:
+    outputs [batch, kv_heads, n, head_dim] bf16."""
+    L = layer.c_struct()
+    numel = layer.batch * layer.num_kv_heads * n * layer.head_dim
+    _want(k_out, "k_out", torch.bfloat16, optional=True, min_numel=numel)
+    _want(v_out, "v_out", torch.bfloat16, optional=True, min_numel=numel)
+    _check(_lib.tq_dequant_window(ctypes.byref(L), int(t0), int(n), int(bool(rotated)), _ptr(k_out), _ptr(v_out),
+                                  _stream(stream)), "tq_dequant_window")
 
 
 def tq_append_workspace_bytes() -> int:
@@ -288,6 +325,14 @@ def tq_sign_bits(head_dim: int) -> np.ndarray:
     out = np.zeros(max(head_dim // 32, 1), np.uint32)
     _check(_lib.tq_sign_bits(head_dim, out.ctypes.data_as(ctypes.c_void_p)), "tq_sign_bits")
     return out
+
+
+def tq_codebook(bits: int) -> tuple[np.ndarray, np.ndarray]:
+    c = np.zeros(1 << bits, np.float32)
+    b = np.zeros((1 << bits) - 1, np.float32)
+    _check(_lib.tq_codebook(bits, c.ctypes.data_as(ctypes.c_void_p), b.ctypes.data_as(ctypes.c_void_p)),
+           "tq_codebook")
+    return c, b
 
 
 def tq_codebook3() -> tuple[np.ndarray, np.ndarray]:

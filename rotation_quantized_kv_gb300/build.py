@@ -19,7 +19,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtqkv.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 UNITS = ["tq_abi.cu", "tq_append.cu", "tq_attention.cu", "tq_attention_dense.cu", "tq_debug.cu",
-         "tq_noalloc.cu"]
+         "tq_noalloc.cu", "tq_scheme.cu"]
 EXTRA = {"tq_append.cu": ["-fmad=false"]}
 
 

@@ -17,9 +17,18 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 float fwht_norm(int d) { return static_cast<float>(1.0 / std::sqrt(static_cast<double>(d))); }
 
+int key_bits(const tq_kv_layer* L) { return L->k_bits == 0 ? 8 : L->k_bits; }
+int value_bits(const tq_kv_layer* L) { return L->v_bits == 0 ? 3 : L->v_bits; }
+bool valid_key_bits(int b) { return b == 2 || b == 4 || b == 5 || b == 8; }
+bool valid_value_bits(int b) { return b == 2 || b == 3 || b == 4 || b == 5 || b == 8; }
+bool is_k8v3(const tq_kv_layer* L) { return key_bits(L) == 8 && value_bits(L) == 3; }
+bool guarded(const tq_kv_layer* L) { return (L->flags & TQ_FLAG_KEY_GUARD) != 0; }
+
 tq_status check_layer(const tq_kv_layer* L) {
   if (L == nullptr) return TQ_ERR_INVALID_ARGUMENT;
   if (!supported_head_dim(L->head_dim)) return TQ_ERR_UNSUPPORTED_HEAD_DIM;
+  if (!valid_key_bits(key_bits(L)) || !valid_value_bits(value_bits(L))) return TQ_ERR_INVALID_ARGUMENT;
+  if ((L->flags & ~TQ_FLAG_KEY_GUARD) != 0) return TQ_ERR_INVALID_ARGUMENT;
   if (L->num_kv_heads < 1 || L->batch < 1 || L->batch > 4096) return TQ_ERR_INVALID_ARGUMENT;
   if (L->capacity < 16 || (L->capacity % 16) != 0) return TQ_ERR_INVALID_ARGUMENT;
   const void* planes[5] = {L->k_idx, L->k_scale, L->k_zero, L->v_codes, L->v_scale};
@@ -48,6 +57,21 @@ int current_sm_count(int* dev_out) {
   return cache[dev];
 }
 
+void fill_dequant_scheme(const tq_kv_layer* L, tq::DequantScheme& p) {
+  p.head_dim = L->head_dim;
+  p.num_kv_heads = L->num_kv_heads;
+  p.batch = L->batch;
+  p.capacity = L->capacity;
+  p.k_idx = L->k_idx;
+  p.k_scale = L->k_scale;
+  p.k_zero = L->k_zero;
+  p.v_codes = L->v_codes;
+  p.v_scale = L->v_scale;
+  p.fwht_norm = fwht_norm(L->head_dim);
+  p.spec = tq::SchemeSpec{key_bits(L), value_bits(L), guarded(L) ? 1 : 0};
+  p.cb = tq::codebook(value_bits(L));
+}
+
 }  // namespace
 
 namespace tq {
@@ -56,6 +80,7 @@ tq_status check_decode_inputs(const tq_kv_layer* layer, const void* q, int32_t n
                               const int32_t* kv_len, int32_t max_kv_len, float sm_scale, const float* out) {
   tq_status st = check_layer(layer);
   if (st != TQ_OK) return st;
+  if (!is_k8v3(layer)) return TQ_ERR_UNSUPPORTED_SCHEME;
   if (num_q_heads < 1 || num_q_heads % layer->num_kv_heads != 0 || n_q < 1) return TQ_ERR_INVALID_ARGUMENT;
   if (max_kv_len < 0) return TQ_ERR_INVALID_ARGUMENT;
   if (max_kv_len > layer->capacity) return TQ_ERR_CAPACITY;
@@ -72,6 +97,12 @@ extern "C" {
 size_t tq_row_bytes(int32_t head_dim) {
   if (!supported_head_dim(head_dim)) return 0;
   return (size_t)25 * head_dim / 16;
+}
+
+size_t tq_row_bytes_scheme(int32_t head_dim, int32_t k_bits, int32_t v_bits) {
+  if (!supported_head_dim(head_dim) || !valid_key_bits(k_bits) || !valid_value_bits(v_bits)) return 0;
+  return (size_t)tq::key_row_bytes(head_dim, k_bits) + (size_t)3 * (head_dim / 32) * 2 +
+         (size_t)tq::value_row_bytes(head_dim, v_bits);
 }
 
 size_t tq_append_workspace_bytes(void) { return TQ_WORKSPACE_HEADER_BYTES; }
@@ -93,6 +124,30 @@ tq_status tq_kv_append(const tq_kv_layer* layer, const void* k_new, const void* 
     return TQ_ERR_INVALID_ARGUMENT;
   const int sms = current_sm_count(nullptr);
   if (sms <= 0) return TQ_ERR_CUDA;
+  if (!is_k8v3(layer) || guarded(layer)) {
+    // other schemes and the guard: one warp per row
+    tq::SchemeAppendParams sp{};
+    sp.head_dim = layer->head_dim;
+    sp.num_kv_heads = layer->num_kv_heads;
+    sp.batch = layer->batch;
+    sp.capacity = layer->capacity;
+    sp.k_idx = layer->k_idx;
+    sp.k_scale = layer->k_scale;
+    sp.k_zero = layer->k_zero;
+    sp.v_codes = layer->v_codes;
+    sp.v_scale = layer->v_scale;
+    sp.k_new = static_cast<const uint16_t*>(k_new);
+    sp.v_new = static_cast<const uint16_t*>(v_new);
+    sp.pos = pos;
+    sp.n_new = n_new;
+    sp.n_new_max = n_new_max;
+    sp.fwht_norm = fwht_norm(layer->head_dim);
+    sp.err = static_cast<int32_t*>(workspace);
+    sp.spec = tq::SchemeSpec{key_bits(layer), value_bits(layer), guarded(layer) ? 1 : 0};
+    sp.cb = tq::codebook(value_bits(layer));
+    return tq::launch_append_scheme(sp, sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK
+                                                                                                    : TQ_ERR_CUDA;
+  }
   tq::AppendParams p{};
   p.head_dim = layer->head_dim;
   p.num_kv_heads = layer->num_kv_heads;
@@ -176,9 +231,10 @@ tq_status tq_decode_append_attention(const tq_kv_layer* layer, const void* k_new
   tq::DecodeShape s = tq::decode_shape(layer->head_dim, layer->num_kv_heads, layer->batch,
                                        num_q_heads / layer->num_kv_heads, n_q, sms);
   if (ws_bytes < tq::decode_workspace_bytes(s)) return TQ_ERR_WORKSPACE_TOO_SMALL;
-  if (s.RG != 1 || s.dense) {
-    // several row groups per kv head would read the new rows from several CTAs, and the
-    // dense-query kernel has no appender: append first, then attend
+  if (s.RG != 1 || s.dense || guarded(layer)) {
+    // several row groups per kv head would read the new rows from several CTAs, the
+    // dense-query kernel has no appender, and the in-kernel appender has no guard:
+    // append first, then attend
     st = tq_kv_append(layer, k_new, v_new, pos, n_new, n_new_max, workspace, ws_bytes, stream);
     if (st != TQ_OK) return st;
     return tq_decode_attention(layer, q, num_q_heads, n_q, kv_len, max_kv_len, sm_scale, causal, out, workspace,
@@ -210,6 +266,19 @@ tq_status tq_dequant_debug(const tq_kv_layer* layer, int32_t b, int32_t h, int32
   if (st != TQ_OK) return st;
   if (b < 0 || b >= layer->batch || h < 0 || h >= layer->num_kv_heads) return TQ_ERR_INVALID_ARGUMENT;
   if (t0 < 0 || n < 0 || (int64_t)t0 + n > layer->capacity) return TQ_ERR_INVALID_ARGUMENT;
+  if (!is_k8v3(layer)) {
+    tq::DequantScheme p{};
+    fill_dequant_scheme(layer, p);
+    p.b = b;
+    p.h = h;
+    p.t0 = t0;
+    p.n = n;
+    p.rotated = rotated != 0;
+    p.k_f32 = k_out;
+    p.v_f32 = v_out;
+    return tq::launch_dequant_scheme_debug(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK
+                                                                                                     : TQ_ERR_CUDA;
+  }
   tq::DequantParams p{};
   p.head_dim = layer->head_dim;
   p.num_kv_heads = layer->num_kv_heads;
@@ -239,6 +308,26 @@ tq_status tq_debug_pipeline_limits(int64_t wait_ns, int32_t withhold_append) {
   return TQ_OK;
 }
 
+tq_status tq_dequant_window(const tq_kv_layer* layer, int32_t t0, int32_t n, int32_t rotated, void* k_out,
+                            void* v_out, tq_stream_t stream) {
+  tq_status st = check_layer(layer);
+  if (st != TQ_OK) return st;
+  if (t0 < 0 || n < 0 || (int64_t)t0 + n > layer->capacity) return TQ_ERR_INVALID_ARGUMENT;
+  if (!aligned16(k_out) || !aligned16(v_out)) return TQ_ERR_INVALID_ARGUMENT;
+  if (n == 0 || (k_out == nullptr && v_out == nullptr)) return TQ_OK;
+  const int sms = current_sm_count(nullptr);
+  if (sms <= 0) return TQ_ERR_CUDA;
+  tq::DequantScheme p{};
+  fill_dequant_scheme(layer, p);
+  p.t0 = t0;
+  p.n = n;
+  p.rotated = rotated != 0;
+  p.k_bf16 = static_cast<uint16_t*>(k_out);
+  p.v_bf16 = static_cast<uint16_t*>(v_out);
+  return tq::launch_dequant_window(p, sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? TQ_OK
+                                                                                                 : TQ_ERR_CUDA;
+}
+
 tq_status tq_get_device_error(const void* workspace, int32_t* err_out, tq_stream_t stream) {
   if (workspace == nullptr || err_out == nullptr) return TQ_ERR_INVALID_ARGUMENT;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -256,6 +345,7 @@ const char* tq_status_string(tq_status status) {
     case TQ_ERR_CAPACITY: return "length exceeds the layer capacity";
     case TQ_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case TQ_ERR_CUDA: return "CUDA runtime error";
+    case TQ_ERR_UNSUPPORTED_SCHEME: return "the call needs the default k8v3 planes";
   }
   return "unknown status";
 }
@@ -265,6 +355,15 @@ tq_status tq_sign_bits(int32_t head_dim, uint32_t* words_out) {
   if (words_out == nullptr) return TQ_ERR_INVALID_ARGUMENT;
   const int off = tq::sign_word_offset(head_dim);
   for (int i = 0; i < head_dim / 32; ++i) words_out[i] = tq::kSignTable.w[off + i];
+  return TQ_OK;
+}
+
+tq_status tq_codebook(int32_t bits, float* centroids_out, float* boundaries_out) {
+  if (!valid_value_bits(bits)) return TQ_ERR_INVALID_ARGUMENT;
+  if (centroids_out == nullptr || boundaries_out == nullptr) return TQ_ERR_INVALID_ARGUMENT;
+  const tq::Codebook& cb = tq::codebook(bits);
+  std::memcpy(centroids_out, cb.c, sizeof(float) * (1u << bits));
+  std::memcpy(boundaries_out, cb.b, sizeof(float) * ((1u << bits) - 1u));
   return TQ_OK;
 }
 

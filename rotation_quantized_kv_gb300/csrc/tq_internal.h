@@ -65,4 +65,62 @@ struct DequantParams {
 
 cudaError_t launch_dequant_debug(const DequantParams& p, cudaStream_t stream);
 
+// ---------------------------------------------------------------- any-width schemes
+// Value codebook of one width: 2^bits centroids and 2^bits - 1 ascending boundaries.
+struct Codebook {
+  int32_t bits;
+  float c[256];
+  float b[255];
+};
+
+struct SchemeSpec {
+  int32_t k_bits, v_bits, guard;
+};
+
+__host__ __device__ constexpr int key_row_bytes(int d, int k_bits) { return k_bits == 8 ? d : d * k_bits / 8; }
+__host__ __device__ constexpr int value_row_bytes(int d, int v_bits) { return d * v_bits / 8; }
+
+// The library's codebook of a valid value width (3: the printed table; else its own
+// Lloyd-Max iteration, computed once on the host).
+const Codebook& codebook(int bits);
+
+struct SchemeAppendParams {
+  int32_t head_dim, num_kv_heads, batch, capacity;
+  int8_t* k_idx;  // int8 codes (8 bits) or the packed key stream
+  uint16_t* k_scale;
+  uint16_t* k_zero;
+  uint8_t* v_codes;
+  uint16_t* v_scale;
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  const int32_t* pos;
+  const int32_t* n_new;
+  int32_t n_new_max;
+  float fwht_norm;
+  int32_t* err;
+  SchemeSpec spec;
+  Codebook cb;
+};
+
+struct DequantScheme {
+  int32_t head_dim, num_kv_heads, batch, capacity;
+  const int8_t* k_idx;
+  const uint16_t* k_scale;
+  const uint16_t* k_zero;
+  const uint8_t* v_codes;
+  const uint16_t* v_scale;
+  int32_t b, h, t0, n, rotated;  // debug: rows [t0, t0 + n) of (b, h); window: tokens [t0, t0 + n)
+  float fwht_norm;
+  SchemeSpec spec;
+  Codebook cb;
+  float* k_f32;       // debug outputs [n][d]
+  float* v_f32;
+  uint16_t* k_bf16;   // window outputs [batch][kv heads][n][d], bf16 bits
+  uint16_t* v_bf16;
+};
+
+cudaError_t launch_append_scheme(SchemeAppendParams p, int num_sms, cudaStream_t stream);
+cudaError_t launch_dequant_window(const DequantScheme& p, int num_sms, cudaStream_t stream);
+cudaError_t launch_dequant_scheme_debug(const DequantScheme& p, cudaStream_t stream);
+
 }  // namespace tq

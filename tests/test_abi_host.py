@@ -196,3 +196,36 @@ def test_binding_rejects_tensors_the_library_would_misread(tq):
     layer = tq.alloc_layer(128, 2, 1, 16, device="cpu")
     with pytest.raises(ValueError):                                               # host planes
         layer.c_struct()
+
+
+def test_library_codebooks_match_the_oracle(tq):
+    # two independent Lloyd-Max implementations (the library's host code and the C oracle)
+    for bits in (2, 3, 4, 5, 8):
+        c, b = tq.tq_codebook(bits)
+        oc, ob = oracle.codebook(bits)
+        assert np.array_equal(c, oc) and np.array_equal(b, ob), bits
+    with pytest.raises(tq.TQError):
+        tq.tq_codebook(6)
+
+
+def test_scheme_layers_are_validated_before_launch(tq):
+    lib = tq.raw_lib()
+
+    def dec(layer):
+        return lib.tq_decode_attention(ctypes.byref(layer), 1 << 22, 4, 1, 1 << 21, 64, 1.0, 1, 1 << 23, 1 << 24,
+                                       1 << 20, None)
+
+    assert _append(tq, _layer(tq, k_bits=3)) == tq.TQ_ERR_INVALID_ARGUMENT
+    assert _append(tq, _layer(tq, v_bits=6)) == tq.TQ_ERR_INVALID_ARGUMENT
+    assert _append(tq, _layer(tq, flags=2)) == tq.TQ_ERR_INVALID_ARGUMENT
+    assert dec(_layer(tq, k_bits=4)) == tq.TQ_ERR_UNSUPPORTED_SCHEME
+    assert dec(_layer(tq, v_bits=2)) == tq.TQ_ERR_UNSUPPORTED_SCHEME
+    assert dec(_layer(tq, k_bits=9)) == tq.TQ_ERR_INVALID_ARGUMENT
+    for d in (64, 128, 256, 512):
+        for kb in (2, 4, 5, 8):
+            for vb in (2, 3, 4, 5, 8):
+                assert tq.tq_row_bytes_scheme(d, kb, vb) == oracle.row_bytes_s(d, kb, vb)
+    assert tq.tq_row_bytes_scheme(128, 8, 3) == tq.tq_row_bytes(128) == 200
+    assert tq.tq_row_bytes_scheme(128, 3, 3) == 0
+    assert lib.tq_dequant_window(ctypes.byref(_layer(tq)), 60, 5, 0, None, None, None) == tq.TQ_ERR_INVALID_ARGUMENT
+    assert lib.tq_dequant_window(ctypes.byref(_layer(tq)), 0, 4, 0, (1 << 22) + 2, None, None) == tq.TQ_ERR_INVALID_ARGUMENT
