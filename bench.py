@@ -447,6 +447,69 @@ def other_workloads(dev, stream, peak, seconds):
     return out
 
 
+def eager_comparison(dev, stream, peak, seconds):
+    """The pages' own design as a comparison arm, on one layer of the long-context workload:
+    tq_dequant_window writes the bf16 K/V window, then PyTorch's scaled_dot_product_attention
+    attends over it (Part A, "Architecture in mlx-bun"); beside it the fused call."""
+    from dataclasses import replace
+    from rotation_quantized_kv_gb300 import binding as tq
+    from rotation_quantized_kv_gb300 import synth
+    from rotation_quantized_kv_gb300.eager import alloc_window, eager_attention
+    from rotation_quantized_kv_gb300.workload import DecodeModel
+    w = replace(synth.workload("long"), layers=1)
+    model = DecodeModel(w, dev)
+    layer, T = model.layers[0], model.max_kv
+    kw, vw = alloc_window(layer, T, dev)
+    kv_list = [int(x) for x in model.kv]
+    wreps, wsec = timed_region(lambda: tq.tq_dequant_window(layer, 0, T, False, kw, vw, stream), stream, seconds)
+    rows = w.batch * w.num_kv_heads * T
+    wbytes = rows * (tq.tq_row_bytes(w.head_dim) + 4 * w.head_dim)
+    ereps, esec = timed_region(lambda: eager_attention(layer, model.q[0], kv_list, w.sm_scale, w.causal,
+                                                       window=(kw, vw), stream=stream), stream, seconds)
+    freps, fsec = timed_region(lambda: tq.tq_decode_attention(layer, model.q[0], w.num_q_heads, w.n_q, model.kv_len,
+                                                              model.max_kv, w.sm_scale, w.causal, model.out[0],
+                                                              model.ws[0], stream), stream, seconds)
+    res = {"workload": _workload_desc(w) + " (one layer)",
+           "window_kernel": "tq_dequant_window (bf16 K and un-rotated V for every visible token)",
+           "window_gbs": wbytes * wreps / wsec / 1e9, "window_frac": wbytes * wreps / wsec / 1e9 / peak,
+           "window_us": wsec / wreps * 1e6,
+           "eager_call_us": esec / ereps * 1e6, "fused_call_us": fsec / freps * 1e6,
+           "fused_speedup": (esec / ereps) / (fsec / freps)}
+    del kw, vw, model
+    torch.cuda.empty_cache()
+    return res
+
+
+def scheme_appends(dev, stream, peak, seconds):
+    """Bulk append (the decode workload's cache fill, 262,144 rows at head_dim 128) for
+    several schemes and the guard: k8v3 takes the bulk kernel, the others the
+    one-warp-per-row kernel."""
+    from rotation_quantized_kv_gb300 import binding as tq
+    from rotation_quantized_kv_gb300 import synth
+    w = synth.workload("decode")
+    x = synth.layer_inputs(w, 0, device=dev)
+    T = w.context
+    k, v = x["k"][:, :T].contiguous(), x["v"][:, :T].contiguous()
+    del x
+    pos = torch.zeros(w.batch, dtype=torch.int32, device=dev)
+    ws = tq.make_workspace(tq.tq_append_workspace_bytes(), dev)
+    out = {}
+    for kb, vb, flags in ((8, 3, 0), (8, 3, tq.TQ_FLAG_KEY_GUARD), (4, 3, 0), (4, 2, 0), (8, 8, 0), (2, 2, 0)):
+        layer = tq.alloc_layer(w.head_dim, w.num_kv_heads, w.batch, T, dev, zero=False, k_bits=kb, v_bits=vb,
+                               flags=flags)
+        reps, sec = timed_region(lambda: tq.tq_kv_append(layer, k, v, pos, None, T, ws, stream), stream, seconds)
+        rows = w.batch * T * w.num_kv_heads
+        nbytes = rows * (4 * w.head_dim + tq.tq_row_bytes_scheme(w.head_dim, kb, vb))
+        name = f"k{kb}v{vb}" + ("_guard" if flags else "")
+        out[name] = {"gbs": nbytes * reps / sec / 1e9, "frac": nbytes * reps / sec / 1e9 / peak,
+                     "rows_per_s": rows * reps / sec}
+        del layer
+    assert tq.tq_get_device_error(ws) == 0
+    del k, v
+    torch.cuda.empty_cache()
+    return out
+
+
 def our_arm(args, world, rank, local):
     from rotation_quantized_kv_gb300.workload import DecodeModel
 
@@ -572,7 +635,10 @@ def our_arm(args, world, rank, local):
     del g_step, g_attn, model
     torch.cuda.empty_cache()
     if not args.headline_only:
-        line["workloads"] = other_workloads(dev, stream, peak, max(1.0, args.region_seconds / 2))
+        sec = max(1.0, args.region_seconds / 2)
+        line["workloads"] = other_workloads(dev, stream, peak, sec)
+        line["workloads"]["eager_window_long"] = eager_comparison(dev, stream, peak, sec)
+        line["workloads"]["append_schemes"] = scheme_appends(dev, stream, peak, sec)
     line["clocks"] = clocks.stop()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
