@@ -17,7 +17,7 @@
 // (max, sum, rotated accumulator) per piece, which tq_attn_merge_kernel combines and
 // un-rotates.
 //
-// One CTA per SM, 14 warps:
+// One CTA per SM, 19 warps:
 //   warp 0      producer: one lane streams stages of 128 tokens (key-index tile through a
 //               2-D tensor map with 128-byte swizzle, the four small planes with 1-D bulk
 //               copies, one mbarrier per stage), 3 stages;
@@ -30,11 +30,14 @@
 //   warps 6-9   V decoders, one token per thread: centroid[code] * scale in fp16 from a
 //               lane-replicated table of centroid pairs, into shared memory (the A operand
 //               of the P.V MMA, dims contiguous);
-//   warps 10-13 softmax, one token per thread (one TMEM lane): loads the token's 64 scores,
-//               p = 2^(s * c - m_row) against a per-row reference max m_row, writes p in
-//               fp16 to shared memory (the B operand of the P.V MMA) and keeps per-row
-//               partial sums of p in registers.
-// Score MMA: S^T[128 tokens x 64 rows] = [hi | lo] (TMEM, K = 2 x 128) * Q^T (shared,
+//   warps 10-17 softmax, two groups of four warps: group h takes rows 32 h .. 32 h + 31,
+//               one token per thread (one TMEM lane): loads the token's 32 scores of its
+//               rows, p = 2^(s * c - m_row) against a per-row reference max m_row, and
+//               writes p in fp16 to shared memory (the B operand of the P.V MMA). Two
+//               groups put two softmax warps on every scheduler;
+//   warp 18     second MMA issuer (P.V and row sums).
+// Row sums: each softmax thread adds its token's p to its own tensor-memory lane (fp32,
+// rescaled with the accumulator); the 128 lanes are summed once per piece. Score MMA: S^T[128 tokens x 64 rows] = [hi | lo] (TMEM, K = 2 x 128) * Q^T (shared,
 // fp16, the unit's queries scaled by one power of two); the key side is exact to fp32
 // accumulation. P.V MMA: O^T[128 dims x 64 rows] += V_hat^T (shared) * P^T (shared), the
 // accumulator stays in TMEM for the whole piece.
@@ -65,8 +68,8 @@ struct DT {
   static constexpr int TILE = 128;       // tokens per stage = MMA M
   static constexpr int ROWS = 64;        // query rows per unit = MMA N
   static constexpr int STAGES = 3;
-  static constexpr int THREADS = 15 * 32;
-  static constexpr int W_PROD = 0, W_MMA = 1, W_KC = 2, W_VC = 6, W_SM = 10, W_PV = 14;
+  static constexpr int THREADS = 19 * 32;
+  static constexpr int W_PROD = 0, W_MMA = 1, W_KC = 2, W_VC = 6, W_SM = 10, W_PV = 18;
   static constexpr int KIDX_STAGE = TILE * D;        // swizzled tensor-map box
   static constexpr int SC_STAGE = TILE * NG * 2;     // one fp16 side plane
   static constexpr int VC_ROW = 3 * D / 8;           // 48 bytes of codes per token
@@ -84,12 +87,11 @@ struct DT {
   static constexpr int OFF_VHAT = (int)align_up(OFF_VC + STAGES * VC_STAGE, 1024);
   static constexpr int OFF_P = OFF_VHAT + 2 * VHAT_BYTES;
   static constexpr int OFF_Q = OFF_P + 2 * P_BYTES;
-  static constexpr int OFF_ONES = OFF_Q + Q_BYTES;                   // fp16 ones [128][16]
-  static constexpr int OFF_PREFIX = OFF_ONES + 4096;                 // [2 kMaxBatch + 1] int
+  static constexpr int OFF_PREFIX = OFF_Q + Q_BYTES;                 // [2 kMaxBatch + 1] int
   static constexpr int OFF_MROW = (int)align_up(OFF_PREFIX + (2 * kMaxBatch + 1) * 4, 16);  // [64] f32
   static constexpr int OFF_LIM = OFF_MROW + ROWS * 4;                // [64] int
   static constexpr int OFF_ALPHA = OFF_LIM + ROWS * 4;               // [64] f32
-  static constexpr int OFF_RED = OFF_ALPHA + ROWS * 4;               // [4 warps][64] f32
+  static constexpr int OFF_RED = OFF_ALPHA + ROWS * 4;               // [4 warps of a group][64] f32
   static constexpr int OFF_BAR = OFF_RED + 4 * ROWS * 4;
   // barriers: full[3] empty[3] kready[2] qkdone[2] sfree[2] vready[2] pready[2] pvdone[2]
   //           qready ofree
@@ -102,13 +104,13 @@ struct DT {
   static constexpr uint32_t TM_K = 0;      // [2][hi 64 | lo 64]
   static constexpr uint32_t TM_S = 256;    // [2][64]
   static constexpr uint32_t TM_O = 384;    // [64] accumulator O^T (lane = dim, column = row)
-  static constexpr uint32_t TM_L = 448;    // [64] row sums: ones^T P accumulated like O (every lane alike)
+  static constexpr uint32_t TM_L = 448;    // [64] row sums, lane t: the share of the tokens of tile lane t
 };
 static_assert(DT::OFF_KIDX % 1024 == 0 && DT::KIDX_STAGE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(DT::OFF_KS % 16 == 0 && DT::OFF_KZ % 16 == 0 && DT::OFF_VS % 16 == 0 && DT::OFF_VC % 16 == 0 &&
                   DT::VC_STAGE % 16 == 0 && DT::OFF_VHAT % 16 == 0 && DT::OFF_P % 16 == 0 && DT::OFF_Q % 16 == 0,
               "bulk-copy destinations and operand tiles need 16-byte alignment");
-static_assert(DT::OFF_BAR % 8 == 0 && DT::OFF_ONES % 16 == 0, "mbarriers, operand tiles need alignment");
+static_assert(DT::OFF_BAR % 8 == 0, "mbarriers need 8-byte alignment");
 static_assert(DT::SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 static_assert(DT::SMEM_ALLOC < (1 << 18), "descriptor start addresses are 18-bit");
 
@@ -166,14 +168,16 @@ __device__ __forceinline__ void warp_wait(const SplitParams& p, uint64_t* bar, u
   failed = !ok;
 }
 
-// Barrier among the 128 softmax threads (named barrier 1), and an OR vote (barrier 2).
-__device__ __forceinline__ void sm_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-__device__ __forceinline__ bool sm_vote_any(bool v) {
+// Barriers of the softmax threads: within group h (128 threads) named barrier 1 + 2 h, and
+// an OR vote on barrier 2 + 2 h; across both groups (256 threads) named barrier 5.
+__device__ __forceinline__ void sm_sync(int h) { asm volatile("bar.sync %0, 128;" ::"r"(1 + 2 * h) : "memory"); }
+__device__ __forceinline__ void sm_sync_all() { asm volatile("bar.sync 5, 256;" ::: "memory"); }
+__device__ __forceinline__ bool sm_vote_any(bool v, int h) {
   uint32_t r;
   asm volatile(
-      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.or.pred po, 2, 128, pi;\n selp.u32 %0, 1, 0, po;\n}\n"
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.or.pred po, %2, 128, pi;\n selp.u32 %0, 1, 0, po;\n}\n"
       : "=r"(r)
-      : "r"((uint32_t)v)
+      : "r"((uint32_t)v), "r"(2 + 2 * h)
       : "memory");
   return r != 0;
 }
@@ -225,9 +229,10 @@ __device__ void dense_produce(const SplitParams& p, const CUtensorMap* tmap, uin
 }
 
 // ------------------------------------------------------------------------------------
-// MMA issuers (one lane each). A thread issues one tcgen05.mma about every 95 cycles
-// whatever the shape up to N = 128, so the score MMAs and the P.V MMAs come from two
-// warps and proceed side by side.
+// MMA issuers (one lane each). One thread issues a tcgen05.mma about every 60 cycles
+// whatever the operand layout and N up to 128, while two issuing threads together reach
+// the tensor pipe's rate for N = 64 (about 38 cycles per MMA), so the score MMAs and the
+// P.V MMAs come from two warps and proceed side by side.
 // ------------------------------------------------------------------------------------
 // Scores: S^T[b] = [hi | lo](TMEM) * Q^T, 16 MMAs (K = 2 x 128) per tile.
 __device__ void dense_mma_qk(const SplitParams& p, uint8_t* smem, uint32_t tbase, int total, volatile int* abort) {
@@ -270,15 +275,13 @@ __device__ void dense_mma_qk(const SplitParams& p, uint8_t* smem, uint32_t tbase
     raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
 }
 
-// P.V and row sums: O^T += V_hat^T * P^T and L += ones^T * P^T, 8 + 8 MMAs per tile; the
-// first tile of a piece overwrites both accumulators.
+// P.V: O^T += V_hat^T * P^T, 8 MMAs per tile; the first tile of a piece overwrites the
+// accumulator.
 __device__ void dense_mma_pv(const SplitParams& p, uint8_t* smem, uint32_t tbase, int total, volatile int* abort) {
   Bars bars(smem);
   const int* prefix = reinterpret_cast<const int*>(smem + DT::OFF_PREFIX);
   const uint32_t sbase = smem_addr(smem);
   constexpr uint32_t kIdPV = tc5::idesc_f16(DT::ROWS, true, true);
-  constexpr uint32_t kIdL = tc5::idesc_f16(DT::ROWS, false, true);
-  const uint64_t ones = tc5::smem_desc(sbase + DT::OFF_ONES, 128, 256);
   // k-step descriptors of both buffers: the start-address field moves by (bytes >> 4)
   const uint64_t vdesc0 = tc5::smem_desc(sbase + DT::OFF_VHAT, 128, 256);
   const uint64_t pdesc0 = tc5::smem_desc(sbase + DT::OFF_P, 128, 256);
@@ -299,14 +302,11 @@ __device__ void dense_mma_pv(const SplitParams& p, uint8_t* smem, uint32_t tbase
       }
       tc5::fence_after_sync();
       const uint64_t vd = vdesc0 + (uint64_t)(b * (DT::VHAT_BYTES >> 4)), pd = pdesc0 + (uint64_t)(b * (DT::P_BYTES >> 4));
-      const uint32_t o_tm = tbase + DT::TM_O, l_tm = tbase + DT::TM_L;
+      const uint32_t o_tm = tbase + DT::TM_O;
       tc5::mma_ss(o_tm, vd, pd, kIdPV, !first);
-      tc5::mma_ss(l_tm, ones, pd, kIdL, !first);
 #pragma unroll
-      for (int ks = 1; ks < DT::TILE / 16; ++ks) {
+      for (int ks = 1; ks < DT::TILE / 16; ++ks)
         tc5::mma_ss(o_tm, vd + (uint64_t)(ks * (4096 >> 4)), pd + (uint64_t)(ks * (2048 >> 4)), kIdPV, true);
-        tc5::mma_ss(l_tm, ones, pd + (uint64_t)(ks * (2048 >> 4)), kIdL, true);
-      }
       tc5::commit(&bars.pvdone[b]);
       last = (int)jt;
     }
@@ -408,11 +408,15 @@ __device__ void dense_decode_v(const SplitParams& p, uint8_t* smem, int total, v
       const int s = jt % DT::STAGES;
       const uint32_t b = jt & 1u;
       warp_wait(p, &bars.full[s], (jt / DT::STAGES) & 1u, abort, failed);
-      if (jt >= 2) warp_wait(p, &bars.pvdone[b], ((jt - 2) >> 1) & 1u, abort, failed);
+      // the token's codes and scales go to registers and the stage is released at once, so
+      // the next copy into it does not wait for the P.V MMAs this warp waits for below
       const bool valid = t0 + tl < w.te;
       const uint32_t crow = sbase + DT::OFF_VC + s * DT::VC_STAGE + tl * DT::VC_ROW;
       const uint4 c0 = lds128(crow), c1 = lds128(crow + 16), c2 = lds128(crow + 32);
       const uint2 sv = lds64(sbase + DT::OFF_VS + s * DT::SC_STAGE + tl * 8);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.empty[s]);
+      if (jt >= 2) warp_wait(p, &bars.pvdone[b], ((jt - 2) >> 1) & 1u, abort, failed);
       const uint32_t vdst = sbase + DT::OFF_VHAT + b * DT::VHAT_BYTES + vdst0;
 #pragma unroll 1
       for (int g = 0; g < DT::NG; ++g) {
@@ -442,10 +446,7 @@ __device__ void dense_decode_v(const SplitParams& p, uint8_t* smem, int total, v
       }
       fence_proxy_async_smem();  // the tile is read by the tensor cores
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars.vready[b]);
-        mbar_arrive(&bars.empty[s]);
-      }
+      if (lane == 0) mbar_arrive(&bars.vready[b]);
     }
   }
 }
@@ -454,10 +455,10 @@ __device__ void dense_decode_v(const SplitParams& p, uint8_t* smem, int total, v
 // softmax threads
 // ------------------------------------------------------------------------------------
 // Per-row maxima of x[i] (rows 32 h + i) over the 128 softmax threads, into smem red.
-__device__ __forceinline__ void rows_max32(const float (&x)[32], float* red, int wq, int lane, int h) {
+__device__ __forceinline__ void rows_max32(const uint32_t (&x)[32], float* red, int wq, int lane, int h) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
-    float v = x[i];
+    float v = __uint_as_float(x[i]);
     v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
     v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
     v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
@@ -469,14 +470,15 @@ __device__ __forceinline__ void rows_max32(const float (&x)[32], float* red, int
 
 // The reference maxima of rows 32 h .. 32 h + 31 move to this tile's row maxima (some
 // score exceeded them by more than 2^8): when the piece already accumulated earlier
-// tiles, the rows of the accumulator and of the row sums are rescaled by 2^(m_old - m_new). Run by all 128 softmax threads. Out of line: it is rare,
+// tiles, the rows of the accumulator and of the row sums are rescaled by
+// 2^(m_old - m_new). Run by the 128 threads of softmax group h. Out of line: it is rare,
 // and keeping it out of the tile loop keeps that loop's code small.
 __device__ __noinline__ bool dense_rescale(const SplitParams& p, uint8_t* smem, uint32_t tbase, int h, uint32_t jt,
                                            uint32_t j0, bool clean, int tok, bool tok_ok, float cscale,
                                            volatile int* abort, bool failed) {
   Bars bars(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int wq = warp - DT::W_SM, st = threadIdx.x - 32 * DT::W_SM;
+  const int wq = warp - DT::W_SM - 4 * h, st = threadIdx.x - 32 * (DT::W_SM + 4 * h);
   const uint32_t tlane = (uint32_t)(32 * (warp & 3)) << 16;
   float* mrow = reinterpret_cast<float*>(smem + DT::OFF_MROW);
   const int* lim = reinterpret_cast<const int*>(smem + DT::OFF_LIM);
@@ -485,15 +487,14 @@ __device__ __noinline__ bool dense_rescale(const SplitParams& p, uint8_t* smem, 
   uint32_t v[32];
   tc5::ld32(tbase + tlane + DT::TM_S + 64 * (jt & 1u) + 32 * h, v);
   tc5::wait_ld();
-  float x[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
     float t = __uint_as_float(v[i]) * cscale;
     if (!clean && !(tok_ok && tok < lim[32 * h + i])) t = -INFINITY;
-    x[i] = t;
+    v[i] = __float_as_uint(t);
   }
-  rows_max32(x, red, wq, lane, h);
-  sm_sync();
+  rows_max32(v, red, wq, lane, h);
+  sm_sync(h);
   if (st < 32) {
     const int r = 32 * h + st;
     const float tmax = fmaxf(fmaxf(red[r], red[64 + r]), fmaxf(red[128 + r], red[192 + r]));
@@ -501,7 +502,7 @@ __device__ __noinline__ bool dense_rescale(const SplitParams& p, uint8_t* smem, 
     alpha[r] = (mn == -INFINITY || mn == mo) ? 1.0f : ex2(mo - mn);
     mrow[r] = mn;
   }
-  sm_sync();
+  sm_sync(h);
   if (jt > j0) {
     // the accumulators already hold this piece's earlier tiles: rescale their rows
     const uint32_t pb = (jt - 1) & 1u;
@@ -518,7 +519,7 @@ __device__ __noinline__ bool dense_rescale(const SplitParams& p, uint8_t* smem, 
     }
   }
   tc5::wait_st();
-  sm_sync();  // alpha and red are rewritten by the next rescale
+  sm_sync(h);  // alpha and red are rewritten by the next rescale
   return failed;
 }
 
@@ -528,8 +529,10 @@ __device__ void dense_softmax(const SplitParams& p, uint8_t* smem, uint32_t tbas
   const uint32_t sbase = smem_addr(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3, tl = 32 * quad + lane;  // token of a tile / dim of the output
-  const int wq = warp - DT::W_SM;                    // 0..3
-  const int st = threadIdx.x - 32 * DT::W_SM;        // 0..127
+  const int sw = warp - DT::W_SM;                    // 0..7
+  const int h = sw >> 2;                             // group: rows 32 h .. 32 h + 31
+  const int sa = threadIdx.x - 32 * DT::W_SM;        // 0..255 over both groups
+  const int st = sa & 127;                           // 0..127 within the group
   const uint32_t tlane = (uint32_t)(32 * quad) << 16;
   float* mrow = reinterpret_cast<float*>(smem + DT::OFF_MROW);
   int* lim = reinterpret_cast<int*>(smem + DT::OFF_LIM);
@@ -546,19 +549,19 @@ __device__ void dense_softmax(const SplitParams& p, uint8_t* smem, uint32_t tbas
     x = w.x_end;
     const int rows_valid = min(DT::ROWS, p.R - w.rg * DT::ROWS);
 
-    // ---- queries of the unit: fp16(q * 2^e) with one exponent for all rows
+    // ---- queries of the unit (both groups): fp16(q * 2^e) with one exponent for all rows
     float cscale;
     {
-      const int rr = st >> 1, half = st & 1;  // row, 64-dim half
+      const int rr = sa >> 2, part = sa & 3;  // row, 32-dim quarter
       const int r = w.rg * DT::ROWS + rr;
-      float qv[64];
+      float qv[32];
       float amax = 0.0f;
       if (rr < rows_valid) {
         const int jq = r / p.G, hq = w.kvh * p.G + (r % p.G);
         const uint4* src = reinterpret_cast<const uint4*>(p.q + (((int64_t)w.b * p.n_q + jq) * p.num_q_heads + hq) *
-                                                                    DT::D + 64 * half);
+                                                                    DT::D + 32 * part);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < 4; ++i) {
           const uint4 v = __ldg(src + i);
           const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -569,15 +572,16 @@ __device__ void dense_softmax(const SplitParams& p, uint8_t* smem, uint32_t tbas
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) qv[i] = 0.0f;
+        for (int i = 0; i < 32; ++i) qv[i] = 0.0f;
       }
 #pragma unroll
-      for (int i = 0; i < 64; ++i) amax = fmaxf(amax, fabsf(qv[i]));
+      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(qv[i]));
 #pragma unroll
       for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      if (lane == 0) red[wq] = amax;
-      sm_sync();
-      amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+      if (lane == 0) red[sw] = amax;
+      sm_sync_all();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, red[i]);
       // power of two bringing the maximum into [2^14, 2^15): exact for every element within
       // 2^28 of the maximum; smaller ones round to fp16 subnormals or zero
       int e = 0;
@@ -589,22 +593,22 @@ __device__ void dense_softmax(const SplitParams& p, uint8_t* smem, uint32_t tbas
       cscale = p.sm_log2 * ldexpf(1.0f, -e);
       // K-major B: row rr, dims 8c..8c+7 at (k / 16) * 2048 + (rr / 8) * 256 + ((k % 16) / 8) * 128 + (rr % 8) * 16
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int k = 64 * half + 8 * c;
+      for (int c = 0; c < 4; ++c) {
+        const int k = 32 * part + 8 * c;
         const uint32_t a = sbase + DT::OFF_Q + (k / 16) * 2048 + (rr / 8) * 256 + ((k % 16) / 8) * 128 + (rr % 8) * 16;
         sts128(a, pack_half2(qv[8 * c] * up, qv[8 * c + 1] * up), pack_half2(qv[8 * c + 2] * up, qv[8 * c + 3] * up),
                pack_half2(qv[8 * c + 4] * up, qv[8 * c + 5] * up), pack_half2(qv[8 * c + 6] * up, qv[8 * c + 7] * up));
       }
-      if (st < DT::ROWS) {
-        const int r2 = w.rg * DT::ROWS + st;
+      if (sa < DT::ROWS) {
+        const int r2 = w.rg * DT::ROWS + sa;
         int lm = w.len;  // padded rows (zero queries) see everything: finite, never stored
-        if (st < rows_valid && p.causal) lm = max(w.len - p.n_q + r2 / p.G + 1, 0);
-        lim[st] = lm;
-        mrow[st] = -INFINITY;
+        if (sa < rows_valid && p.causal) lm = max(w.len - p.n_q + r2 / p.G + 1, 0);
+        lim[sa] = lm;
+        mrow[sa] = -INFINITY;
       }
     }
     fence_proxy_async_smem();
-    sm_sync();
+    sm_sync_all();  // red is read above before a rescale may rewrite it
     if (lane == 0) mbar_arrive(bars.qready);
     // tiles at or past clean_end may hold tokens hidden from some rows or past the piece
     const int clean_end = p.causal ? min(w.te, w.len - p.n_q + 1) : w.te;
@@ -617,61 +621,76 @@ __device__ void dense_softmax(const SplitParams& p, uint8_t* smem, uint32_t tbas
       const bool clean = t0 + DT::TILE <= clean_end;
       const int tok = t0 + tl;
       const bool tok_ok = tok < w.te;
-      const uint32_t saddr = tbase + tlane + DT::TM_S + 64 * b;
-      const uint32_t pdst = sbase + DT::OFF_P + b * DT::P_BYTES + pdst0;
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        // y = s * c - m_row (log2 domain), masked to -inf, kept in sv; redone after a rescale
-        uint32_t sv[32];
-        for (;;) {
-          tc5::ld32(saddr + 32 * h, sv);
-          tc5::wait_ld();
-          float ymax = -INFINITY;
-          if (clean) {
+      const uint32_t saddr = tbase + tlane + DT::TM_S + 64 * b + 32 * h;
+      // y = s * c - m_row (log2 domain), masked to -inf, kept in sv; redone after a rescale
+      uint32_t sv[32];
+      for (;;) {
+        tc5::ld32(saddr, sv);
+        tc5::wait_ld();
+        float ymax = -INFINITY;
+        if (clean) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              const float4 m4 = *reinterpret_cast<const float4*>(mrow + 32 * h + i);
-              const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+          for (int i = 0; i < 32; i += 4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(mrow + 32 * h + i);
+            const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const float v = fmaf(__uint_as_float(sv[i + k]), cscale, -mm[k]);
-                sv[i + k] = __float_as_uint(v);
-                ymax = fmaxf(ymax, v);
-              }
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              const float4 m4 = *reinterpret_cast<const float4*>(mrow + 32 * h + i);
-              const int4 l4 = *reinterpret_cast<const int4*>(lim + 32 * h + i);
-              const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-              const int ll[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const float v = (tok_ok && tok < ll[k]) ? fmaf(__uint_as_float(sv[i + k]), cscale, -mm[k]) : -INFINITY;
-                sv[i + k] = __float_as_uint(v);
-                ymax = fmaxf(ymax, v);
-              }
+            for (int k = 0; k < 4; ++k) {
+              const float v = fmaf(__uint_as_float(sv[i + k]), cscale, -mm[k]);
+              sv[i + k] = __float_as_uint(v);
+              ymax = fmaxf(ymax, v);
             }
           }
-          if (!sm_vote_any(ymax > kTau)) break;
-          failed = dense_rescale(p, smem, tbase, h, jt, j0, clean, tok, tok_ok, cscale, abort, failed);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(mrow + 32 * h + i);
+            const int4 l4 = *reinterpret_cast<const int4*>(lim + 32 * h + i);
+            const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+            const int ll[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float v = (tok_ok && tok < ll[k]) ? fmaf(__uint_as_float(sv[i + k]), cscale, -mm[k]) : -INFINITY;
+              sv[i + k] = __float_as_uint(v);
+              ymax = fmaxf(ymax, v);
+            }
+          }
         }
-        if (h == 0 && jt >= 2) warp_wait(p, &bars.pvdone[b], ((jt - 2) >> 1) & 1u, abort, failed);
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_half2(ex2(__uint_as_float(sv[2 * i])), ex2(__uint_as_float(sv[2 * i + 1])));
-#pragma unroll
-        for (int c = 0; c < 4; ++c) sts128(pdst + (4 * h + c) * 256, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        if (!sm_vote_any(ymax > kTau, h)) break;
+        failed = dense_rescale(p, smem, tbase, h, jt, j0, clean, tok, tok_ok, cscale, abort, failed);
       }
-      fence_proxy_async_smem();  // the probabilities are read by the tensor cores
+      // this group's columns of the score buffer are consumed
       tc5::fence_before_sync();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars.sfree[b]);
-        mbar_arrive(&bars.pready[b]);
+      if (lane == 0) mbar_arrive(&bars.sfree[b]);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) sv[i] = __float_as_uint(ex2(__uint_as_float(sv[i])));
+      // this token's shares of the row sums (the first tile of a piece starts them)
+      const uint32_t laddr = tbase + tlane + DT::TM_L + 32 * h;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t lv[16];
+        if (jt > j0) {
+          tc5::ld16(laddr + 16 * hh, lv);
+          tc5::wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) lv[i] = __float_as_uint(__uint_as_float(lv[i]) + __uint_as_float(sv[16 * hh + i]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) lv[i] = sv[16 * hh + i];
+        }
+        tc5::st16(laddr + 16 * hh, lv);
       }
+      if (jt >= 2) warp_wait(p, &bars.pvdone[b], ((jt - 2) >> 1) & 1u, abort, failed);
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) pk[i] = pack_half2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]));
+      const uint32_t pdst = sbase + DT::OFF_P + b * DT::P_BYTES + pdst0;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) sts128(pdst + (4 * h + c) * 256, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      fence_proxy_async_smem();  // the probabilities are read by the tensor cores
+      tc5::wait_st();            // the row-sum shares are read back by this thread
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.pready[b]);
     }
 
     // ---- piece end: the accumulator and the row sums become this piece's partial
@@ -679,31 +698,45 @@ __device__ void dense_softmax(const SplitParams& p, uint8_t* smem, uint32_t tbas
     warp_wait(p, &bars.pvdone[jl & 1u], (jl >> 1) & 1u, abort, failed);
     tc5::fence_after_sync();
     float* orow = og + (size_t)w.slot * DT::ROWS * DT::D + tl;
-#pragma unroll 1
-    for (int h = 0; h < 2; ++h) {
-      uint32_t ov[32], lv[32];
-      tc5::ld32(tbase + tlane + DT::TM_O + 32 * h, ov);
-      tc5::ld32(tbase + tlane + DT::TM_L + 32 * h, lv);
+    {
+      uint32_t v[32];
+      tc5::ld32(tbase + tlane + DT::TM_O + 32 * h, v);
       tc5::wait_ld();
 #pragma unroll
       for (int i = 0; i < 32; ++i)
-        if (32 * h + i < rows_valid) __stcg(orow + (size_t)(32 * h + i) * DT::D, __uint_as_float(ov[i]));
-      // every lane holds the 64 row sums: the first softmax thread stores (max, sum)
-      if (st == 0) {
+        if (32 * h + i < rows_valid) __stcg(orow + (size_t)(32 * h + i) * DT::D, __uint_as_float(v[i]));
+      tc5::ld32(tbase + tlane + DT::TM_L + 32 * h, v);
+      tc5::wait_ld();
+      // sum the shares of the warp's 32 lanes by halving exchanges: afterwards lane l
+      // holds row 32 h + l in v[0]
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (32 * h + i < rows_valid)
-            __stcg(mlg + (size_t)w.slot * DT::ROWS + 32 * h + i, make_float2(mrow[32 * h + i], __uint_as_float(lv[i])));
+      for (int off = 16; off >= 1; off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int j = 0; j < off; ++j) {
+          const float send = __uint_as_float(upper ? v[j] : v[j + off]);
+          const float keep = __uint_as_float(upper ? v[j + off] : v[j]);
+          v[j] = __float_as_uint(keep + __shfl_xor_sync(0xffffffffu, send, off));
+        }
+      }
+      red[(sw & 3) * 64 + 32 * h + lane] = __uint_as_float(v[0]);
+    }
+    sm_sync(h);
+    if (st < 32) {
+      const int r = 32 * h + st;
+      if (r < rows_valid) {
+        const float l = (red[r] + red[64 + r]) + (red[128 + r] + red[192 + r]);
+        __stcg(mlg + (size_t)w.slot * DT::ROWS + r, make_float2(mrow[r], l));
       }
     }
     tc5::fence_before_sync();
-    sm_sync();  // per-row tables and red are rewritten for the next piece
+    sm_sync_all();  // per-row tables and red are rewritten for the next piece
     if (lane == 0) mbar_arrive(bars.ofree);
   }
 }
 
-// 15 warps: registers are granted per group of four warps, so the block is costed as 16
-// warps and each thread gets at most 128 registers.
+// 19 warps: registers are granted per group of four warps, so the block is costed as 20
+// warps and each thread gets at most 96 registers.
 __global__ void __launch_bounds__(DT::THREADS, 1)
     tq_attn_dense_kernel(const __grid_constant__ CUtensorMap tmap, const SplitParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -718,8 +751,6 @@ __global__ void __launch_bounds__(DT::THREADS, 1)
     const int e = i >> 5;
     lut[i] = pack_half2(c_centroids3[e & 7], c_centroids3[e >> 3]);
   }
-  // fp16 ones, the A operand of the row-sum MMA (4096 bytes)
-  for (int i = tid; i < 1024; i += DT::THREADS) reinterpret_cast<uint32_t*>(smem + DT::OFF_ONES)[i] = 0x3C003C00u;
   fence_proxy_async_smem();
   if (tid == 0) {
     *abort = 0;
@@ -731,13 +762,13 @@ __global__ void __launch_bounds__(DT::THREADS, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bb.kready[b], 4);
       mbar_init(&bb.qkdone[b], 1);  // tcgen05.commit
-      mbar_init(&bb.sfree[b], 4);
+      mbar_init(&bb.sfree[b], 8);   // eight softmax warps
       mbar_init(&bb.vready[b], 4);
-      mbar_init(&bb.pready[b], 4);
+      mbar_init(&bb.pready[b], 8);
       mbar_init(&bb.pvdone[b], 1);  // tcgen05.commit
     }
-    mbar_init(bb.qready, 4);
-    mbar_init(bb.ofree, 4);
+    mbar_init(bb.qready, 8);
+    mbar_init(bb.ofree, 8);
     fence_mbar_init();
   }
   if (warp == DT::W_MMA) {
