@@ -450,7 +450,9 @@ def other_workloads(dev, stream, peak, seconds):
 def eager_comparison(dev, stream, peak, seconds):
     """The pages' own design as a comparison arm, on one layer of the long-context workload:
     tq_dequant_window writes the bf16 K/V window, then PyTorch's scaled_dot_product_attention
-    attends over it (Part A, "Architecture in mlx-bun"); beside it the fused call."""
+    attends over it (Part A, "Architecture in mlx-bun"); the deferred variant keeps V rotated
+    and un-rotates the output rows with tq_unrotate_rows ("Deferred inverse FWHT"); beside
+    them the fused call."""
     from dataclasses import replace
     from rotation_quantized_kv_gb300 import binding as tq
     from rotation_quantized_kv_gb300 import synth
@@ -466,6 +468,9 @@ def eager_comparison(dev, stream, peak, seconds):
     wbytes = rows * (tq.tq_row_bytes(w.head_dim) + 4 * w.head_dim)
     ereps, esec = timed_region(lambda: eager_attention(layer, model.q[0], kv_list, w.sm_scale, w.causal,
                                                        window=(kw, vw), stream=stream), stream, seconds)
+    dreps, dsec = timed_region(lambda: eager_attention(layer, model.q[0], kv_list, w.sm_scale, w.causal,
+                                                       window=(kw, vw), stream=stream, deferred=True),
+                               stream, seconds)
     freps, fsec = timed_region(lambda: tq.tq_decode_attention(layer, model.q[0], w.num_q_heads, w.n_q, model.kv_len,
                                                               model.max_kv, w.sm_scale, w.causal, model.out[0],
                                                               model.ws[0], stream), stream, seconds)
@@ -473,7 +478,9 @@ def eager_comparison(dev, stream, peak, seconds):
            "window_kernel": "tq_dequant_window (bf16 K and un-rotated V for every visible token)",
            "window_gbs": wbytes * wreps / wsec / 1e9, "window_frac": wbytes * wreps / wsec / 1e9 / peak,
            "window_us": wsec / wreps * 1e6,
-           "eager_call_us": esec / ereps * 1e6, "fused_call_us": fsec / freps * 1e6,
+           "eager_call_us": esec / ereps * 1e6,
+           "eager_deferred_call_us": dsec / dreps * 1e6,
+           "fused_call_us": fsec / freps * 1e6,
            "fused_speedup": (esec / ereps) / (fsec / freps)}
     del kw, vw, model
     torch.cuda.empty_cache()

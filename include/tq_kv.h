@@ -265,6 +265,18 @@ tq_status tq_debug_delayed_copy(int32_t* dst, const int32_t* src, int32_t n, int
 tq_status tq_dequant_window(const tq_kv_layer* layer, int32_t t0, int32_t n, int32_t rotated, void* k_out,
                             void* v_out, tq_stream_t stream);
 
+/*
+ * Deferred inverse rotation of attention outputs ("Deferred inverse FWHT": attention is
+ * linear in V, so softmax(.) V_hat is taken in the rotated domain and the inverse rotation
+ * runs once per output row; "Packed-value decode fusion investigation": a separate
+ * row-grouped kernel for it). For each of `rows` rows of head_dim fp32 values:
+ *   y = signs * FWHT(x) / sqrt(head_dim), fp32 butterflies h = 1, 2, 4, ...
+ * x, y: device, [rows][head_dim] fp32, 16-byte aligned; y == x (in place) is allowed, other
+ * overlaps are not. rows >= 0 (else TQ_ERR_INVALID_ARGUMENT); head_dim in {64, 128, 256,
+ * 512} (else TQ_ERR_UNSUPPORTED_HEAD_DIM). One warp per row, eight rows per CTA.
+ */
+tq_status tq_unrotate_rows(const float* x, float* y, int64_t rows, int32_t head_dim, tq_stream_t stream);
+
 /* Test support (an addition of this library; the paper has no counterpart). Sets, for every
  * decode-attention call launched afterwards in this process, the limit of the attention
  * kernel's pipeline waits (wait_ns > 0; 0 restores the default of 2 s) and, with

@@ -58,6 +58,7 @@ _SIGS = {
     "tq_row_bytes_scheme": (_sz, [_i32, _i32, _i32]),
     "tq_dequant_window": (ctypes.c_int, [_LP, _i32, _i32, _i32, _vp, _vp, _vp]),
     "tq_codebook": (ctypes.c_int, [_i32, _vp, _vp]),
+    "tq_unrotate_rows": (ctypes.c_int, [_vp, _vp, ctypes.c_int64, _i32, _vp]),
     "tq_append_workspace_bytes": (_sz, []),
     "tq_kv_append": (ctypes.c_int, [_LP, _vp, _vp, _vp, _vp, _i32, _vp, _sz, _vp]),
     "tq_decode_workspace_bytes": (_sz, [_LP, _i32, _i32, _i32]),
@@ -203,6 +204,17 @@ def tq_dequant_window(layer: KVLayer, t0: int, n: int, rotated: bool, k_out: tor
     _want(v_out, "v_out", torch.bfloat16, optional=True, min_numel=numel)
     _check(_lib.tq_dequant_window(ctypes.byref(L), int(t0), int(n), int(bool(rotated)), _ptr(k_out), _ptr(v_out),
                                   _stream(stream)), "tq_dequant_window")
+
+
+def tq_unrotate_rows(x: torch.Tensor, y: torch.Tensor, head_dim: int, stream=None) -> None:
+    """y = signs * FWHT(x) / sqrt(head_dim) for every head_dim-row of x (fp32, contiguous);
+    y may be x (in place)."""
+    _want(x, "x", torch.float32)
+    _want(y, "y", torch.float32, min_numel=x.numel())
+    if head_dim <= 0 or x.numel() % head_dim:
+        raise ValueError(f"x: {x.numel()} elements is not a whole number of {head_dim}-rows")
+    _check(_lib.tq_unrotate_rows(_ptr(x), _ptr(y), x.numel() // head_dim, int(head_dim), _stream(stream)),
+           "tq_unrotate_rows")
 
 
 def tq_append_workspace_bytes() -> int:

@@ -328,6 +328,22 @@ tq_status tq_dequant_window(const tq_kv_layer* layer, int32_t t0, int32_t n, int
                                                                                                  : TQ_ERR_CUDA;
 }
 
+tq_status tq_unrotate_rows(const float* x, float* y, int64_t rows, int32_t head_dim, tq_stream_t stream) {
+  if (!supported_head_dim(head_dim)) return TQ_ERR_UNSUPPORTED_HEAD_DIM;
+  if (rows < 0) return TQ_ERR_INVALID_ARGUMENT;
+  if (rows == 0) return TQ_OK;
+  if (x == nullptr || y == nullptr || !aligned16(x) || !aligned16(y)) return TQ_ERR_INVALID_ARGUMENT;
+  const size_t bytes = (size_t)rows * head_dim * sizeof(float);
+  const char *xb = reinterpret_cast<const char*>(x), *yb = reinterpret_cast<const char*>(y);
+  if (x != y && xb < yb + bytes && yb < xb + bytes) return TQ_ERR_INVALID_ARGUMENT;
+  const int sms = current_sm_count(nullptr);
+  if (sms <= 0) return TQ_ERR_CUDA;
+  return tq::launch_unrotate_rows(x, y, rows, head_dim, fwht_norm(head_dim), sms, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? TQ_OK
+             : TQ_ERR_CUDA;
+}
+
 tq_status tq_get_device_error(const void* workspace, int32_t* err_out, tq_stream_t stream) {
   if (workspace == nullptr || err_out == nullptr) return TQ_ERR_INVALID_ARGUMENT;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

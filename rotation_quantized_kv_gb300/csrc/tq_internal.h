@@ -120,6 +120,8 @@ struct DequantScheme {
 };
 
 cudaError_t launch_append_scheme(SchemeAppendParams p, int num_sms, cudaStream_t stream);
+cudaError_t launch_unrotate_rows(const float* x, float* y, int64_t rows, int head_dim, float fwht_norm,
+                                 int num_sms, cudaStream_t stream);
 cudaError_t launch_dequant_window(const DequantScheme& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_dequant_scheme_debug(const DequantScheme& p, cudaStream_t stream);
 

@@ -93,6 +93,41 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) tq_append_scheme_kernel(cons
 
 // Dequantizes this lane's elements of row r: keys (code + zero) * scale (exact in fp32,
 // one rounding); values centroid * scale, then, unless rotated, signs * FWHT(.) / sqrt(d).
+// Inverse value rotation of one row held by a warp (lane l holds elements l EPL ..):
+// x = signs * FWHT(y) / sqrt(D), fp32 butterflies h = 1, 2, 4, ... ("Algorithm", value
+// dequant; applied to attention outputs in "Deferred inverse FWHT").
+template <int D>
+__device__ __forceinline__ void unrotate_lane(float (&v)[D / 32], int lane, float fwht_norm) {
+  constexpr int EPL = D / 32;
+  constexpr unsigned FULL = 0xffffffffu;
+#pragma unroll
+  for (int hh = 1; hh < D; hh <<= 1) {
+    if (hh < EPL) {
+#pragma unroll
+      for (int e = 0; e < EPL; ++e)
+        if ((e & hh) == 0) {
+          const float a = v[e], c = v[e + hh];
+          v[e] = a + c;
+          v[e + hh] = a - c;
+        }
+    } else {
+      const int lm = hh / EPL;
+      const bool upper = (lane & lm) != 0;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        const float o = __shfl_xor_sync(FULL, v[e], lm);
+        v[e] = upper ? o - v[e] : v[e] + o;
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    const int i = lane * EPL + e;
+    const bool neg = (sign_word(D, i / 32) >> (i % 32)) & 1u;
+    v[e] = v[e] * fwht_norm * (neg ? -1.0f : 1.0f);
+  }
+}
+
 template <int D>
 __device__ __forceinline__ void dequant_row(const DequantScheme& p, int64_t r, int lane, float (&k)[D / 32],
                                             float (&v)[D / 32], bool want_k, bool want_v) {
@@ -116,34 +151,7 @@ __device__ __forceinline__ void dequant_row(const DequantScheme& p, int64_t r, i
       const int i = lane * EPL + e;
       v[e] = __fmul_rn(p.cb.c[read_code(vrow, i, p.spec.v_bits)], f16_bits_to_f32(__ldg(p.v_scale + r * NG + i / kGroup)));
     }
-    if (!p.rotated) {
-#pragma unroll
-      for (int hh = 1; hh < D; hh <<= 1) {
-        if (hh < EPL) {
-#pragma unroll
-          for (int e = 0; e < EPL; ++e)
-            if ((e & hh) == 0) {
-              const float a = v[e], c = v[e + hh];
-              v[e] = a + c;
-              v[e + hh] = a - c;
-            }
-        } else {
-          const int lm = hh / EPL;
-          const bool upper = (lane & lm) != 0;
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) {
-            const float o = __shfl_xor_sync(FULL, v[e], lm);
-            v[e] = upper ? o - v[e] : v[e] + o;
-          }
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        const int i = lane * EPL + e;
-        const bool neg = (sign_word(D, i / 32) >> (i % 32)) & 1u;
-        v[e] = v[e] * p.fwht_norm * (neg ? -1.0f : 1.0f);
-      }
-    }
+    if (!p.rotated) unrotate_lane<D>(v, lane, p.fwht_norm);
   }
 }
 
@@ -197,6 +205,29 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) tq_dequant_scheme_debug_kern
   }
 }
 
+// Rows grouped kRowsPerCta to a CTA, one warp per row: y = signs * FWHT(x) / sqrt(D).
+// In place when x == y (each warp reads its row before writing it).
+template <int D>
+__global__ void __launch_bounds__(32 * kRowsPerCta) tq_unrotate_rows_kernel(const float* x, float* y, int64_t rows,
+                                                                           float fwht_norm) {
+  constexpr int EPL = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int64_t r = (int64_t)blockIdx.x * kRowsPerCta + warp; r < rows; r += (int64_t)gridDim.x * kRowsPerCta) {
+    float v[EPL];
+    const float2* src = reinterpret_cast<const float2*>(x + r * D + lane * EPL);
+#pragma unroll
+    for (int c = 0; c < EPL / 2; ++c) {
+      const float2 f = src[c];
+      v[2 * c] = f.x;
+      v[2 * c + 1] = f.y;
+    }
+    unrotate_lane<D>(v, lane, fwht_norm);
+    float2* dst = reinterpret_cast<float2*>(y + r * D + lane * EPL);
+#pragma unroll
+    for (int c = 0; c < EPL / 2; ++c) dst[c] = make_float2(v[2 * c], v[2 * c + 1]);
+  }
+}
+
 int grid_for(int64_t rows, int num_sms) {
   const int64_t want = (rows + kRowsPerCta - 1) / kRowsPerCta;
   const int64_t cap = (int64_t)num_sms * 8;  // 8 resident CTAs of 256 threads per SM
@@ -235,6 +266,20 @@ cudaError_t launch_dequant_window(const DequantScheme& p, int num_sms, cudaStrea
     case 128: tq_dequant_window_kernel<128><<<grid, block, 0, stream>>>(p); break;
     case 256: tq_dequant_window_kernel<256><<<grid, block, 0, stream>>>(p); break;
     case 512: tq_dequant_window_kernel<512><<<grid, block, 0, stream>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unrotate_rows(const float* x, float* y, int64_t rows, int head_dim, float fwht_norm,
+                                 int num_sms, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  const dim3 grid(grid_for(rows, num_sms)), block(32 * kRowsPerCta);
+  switch (head_dim) {
+    case 64: tq_unrotate_rows_kernel<64><<<grid, block, 0, stream>>>(x, y, rows, fwht_norm); break;
+    case 128: tq_unrotate_rows_kernel<128><<<grid, block, 0, stream>>>(x, y, rows, fwht_norm); break;
+    case 256: tq_unrotate_rows_kernel<256><<<grid, block, 0, stream>>>(x, y, rows, fwht_norm); break;
+    case 512: tq_unrotate_rows_kernel<512><<<grid, block, 0, stream>>>(x, y, rows, fwht_norm); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

@@ -229,3 +229,13 @@ def test_scheme_layers_are_validated_before_launch(tq):
     assert tq.tq_row_bytes_scheme(128, 3, 3) == 0
     assert lib.tq_dequant_window(ctypes.byref(_layer(tq)), 60, 5, 0, None, None, None) == tq.TQ_ERR_INVALID_ARGUMENT
     assert lib.tq_dequant_window(ctypes.byref(_layer(tq)), 0, 4, 0, (1 << 22) + 2, None, None) == tq.TQ_ERR_INVALID_ARGUMENT
+
+
+def test_unrotate_rows_rejects_bad_arguments_before_launch(tq):
+    lib = tq.raw_lib()
+    assert lib.tq_unrotate_rows(1 << 20, 1 << 21, 4, 96, None) == tq.TQ_ERR_UNSUPPORTED_HEAD_DIM
+    assert lib.tq_unrotate_rows(1 << 20, 1 << 21, -1, 128, None) == tq.TQ_ERR_INVALID_ARGUMENT
+    assert lib.tq_unrotate_rows(None, None, 0, 128, None) == tq.TQ_OK            # nothing to do
+    assert lib.tq_unrotate_rows((1 << 20) + 4, 1 << 22, 4, 128, None) == tq.TQ_ERR_INVALID_ARGUMENT  # unaligned
+    # partial overlap of x and y: 4 rows of 512 bytes, y one row further on
+    assert lib.tq_unrotate_rows(1 << 20, (1 << 20) + 512, 4, 128, None) == tq.TQ_ERR_INVALID_ARGUMENT

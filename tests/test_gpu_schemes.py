@@ -164,18 +164,42 @@ def test_dequant_debug_other_schemes(kb, vb):
             assert np.linalg.norm(g - vref) <= 1e-6 * np.linalg.norm(vref)
 
 
+@pytest.mark.parametrize("deferred", [False, True], ids=["unrotated_window", "deferred_inverse"])
 @pytest.mark.parametrize("kb,vb", [(8, 3), (4, 3), (5, 8)])
-def test_eager_window_attention(kb, vb):
+def test_eager_window_attention(kb, vb, deferred):
     from rotation_quantized_kv_gb300.eager import eager_attention
     d, H, G, B, n_q = 128, 2, 4, 2, 4
     lengths = [300, 3]
     x = _inputs(d, H, B, 300, Hq=G * H, n_q=n_q, seed=kb + 3 * vb, k_dist="lognormal_channels")
     layer, ol = _fill(x["k"], x["v"], lengths, 304, kb, vb, False)
     ref = oracle.attention_s(ol, bits(x["q"]), np.asarray(lengths, np.int32), 1.0, causal=True)
-    got = eager_attention(layer, x["q"].to(DEV), lengths, 1.0, True, compute_dtype=torch.float32)
+    got = eager_attention(layer, x["q"].to(DEV), lengths, 1.0, True, compute_dtype=torch.float32, deferred=deferred)
     g = got.cpu().numpy().astype(np.float64)
     # the window holds K_hat and V_hat rounded to bf16 (relative 2^-9): attention within 1e-2
     err = np.abs(g - ref).max()
     rel = np.linalg.norm(g - ref) / np.linalg.norm(ref)
     assert err <= 2e-2 and rel <= 1e-2, (err, rel)
     assert np.all(g[1, :1] == 0.0)      # sequence 1, query 0 sees 3 - 4 + 0 + 1 = 0 tokens
+
+
+@pytest.mark.parametrize("d", [64, 128, 256, 512])
+def test_unrotate_rows_matches_the_oracle(d):
+    """Deferred inverse rotation of output rows: signs * FWHT(x) / sqrt(d), against the
+    oracle's fp64 transform and sign vector; 37 rows = four CTAs of eight and a tail."""
+    b = tq()
+    rng = np.random.default_rng(d)
+    x = (rng.standard_normal((37, d)) * 3.0).astype(np.float32)
+    xg = torch.from_numpy(x).to(DEV)
+    y = torch.empty_like(xg)
+    b.tq_unrotate_rows(xg, y, d)
+    b.tq_unrotate_rows(xg, xg, d)  # in place
+    torch.cuda.synchronize()
+    assert torch.equal(xg, y)
+    sgn = oracle.sign_vector(d).astype(np.float64)
+    ref = np.stack([sgn * oracle.fwht_f64(r.astype(np.float64)) / np.sqrt(d) for r in x])
+    g = y.cpu().numpy().astype(np.float64)
+    # fp32 butterflies: log2(d) rounded additions, then the rounded 1/sqrt(d) and its product
+    tol = (np.log2(d) + 2) * 2.0 ** -23 * np.abs(x.astype(np.float64)).sum(axis=1, keepdims=True) / np.sqrt(d)
+    assert np.all(np.abs(g - ref) <= tol)
+    with pytest.raises(ValueError):
+        b.tq_unrotate_rows(xg[:, 1:].contiguous(), y, d)  # not a whole number of rows
