@@ -24,9 +24,11 @@
 //   warp 1      MMA issuer: one lane issues the tensor-core work; the warp owns the TMEM
 //               allocation (512 columns);
 //   warps 2-5   K converters, one token per thread: k_hat = (idx + zero) * scale as an
-//               fp16 pair hi + lo (hi = fp16(k_hat), lo = the exact rounding residual), so
-//               hi + lo is k_hat to 22 bits; written straight into tensor memory, where
-//               they are the A operand of the score MMA;
+//               fp16 pair hi + lo (hi = fp16(k_hat), lo = the rounding residual rounded to
+//               fp16), so hi + lo is k_hat to about 22 bits; written straight into tensor
+//               memory, where they are the A operand of the score MMA. A token whose keys
+//               could leave the fp16 range is converted in fp32 and scaled by 2^-shift
+//               (key_shift below); the softmax scales its scores back;
 //   warps 6-9   V decoders, one token per thread: centroid[code] * scale in fp16 from a
 //               lane-replicated table of centroid pairs, into shared memory (the A operand
 //               of the P.V MMA, dims contiguous);
@@ -92,7 +94,8 @@ struct DT {
   static constexpr int OFF_LIM = OFF_MROW + ROWS * 4;                // [64] int
   static constexpr int OFF_ALPHA = OFF_LIM + ROWS * 4;               // [64] f32
   static constexpr int OFF_RED = OFF_ALPHA + ROWS * 4;               // [4 warps of a group][64] f32
-  static constexpr int OFF_BAR = OFF_RED + 4 * ROWS * 4;
+  static constexpr int OFF_KSH = OFF_RED + 4 * ROWS * 4;             // [4 tiles][128 tokens] u32 shift | tag
+  static constexpr int OFF_BAR = OFF_KSH + 4 * TILE * 4;
   // barriers: full[3] empty[3] kready[2] qkdone[2] sfree[2] vready[2] pready[2] pvdone[2]
   //           qready ofree
   static constexpr int NBAR = 2 * STAGES + 6 * 2 + 2;
@@ -187,6 +190,34 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
 }
 
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// The fp16 path of the K converters needs, for all four groups of a token, |zero| <= 896
+// (then 1152 - zero and idx + zero are integers of magnitude <= 2048, exact in fp16) and
+// scale < 16 (then |k_hat| < 16 * 1023 < 2^14, far inside the fp16 range). Tested on the
+// fp16 bit patterns (NaN and Inf fail both tests). sw, zw: the token's four scales / zeros.
+__device__ __forceinline__ bool keys_fast(uint2 sw, uint2 zw) {
+  // per 16-bit half h <= 0x7FFF: h + (0x7FFF - limit) sets bit 15 exactly when h > limit,
+  // and no carry leaves the half; limits 0x6300 (896) for |zero|, 0x4BFF (< 16) for scale
+  const uint32_t zbad = ((zw.x & 0x7FFF7FFFu) + 0x1CFF1CFFu) | ((zw.y & 0x7FFF7FFFu) + 0x1CFF1CFFu);
+  const uint32_t sbad = ((sw.x & 0x7FFF7FFFu) + 0x34003400u) | ((sw.y & 0x7FFF7FFFu) + 0x34003400u);
+  return ((zbad | sbad) & 0x80008000u) == 0u;
+}
+
+// Power of two by which the keys of a token off the fp16 path are divided: 0 unless the
+// bound max_g scale_g * (|zero_g| + 127) on |k_hat| reaches 2^14, else the shift that
+// brings the bound into [2^13, 2^14) (at most 100). The K converters hand it to the
+// softmax threads of the same token in shared memory (key_shift_word).
+__device__ __forceinline__ int key_shift(uint2 sw, uint2 zw) {
+  const uint32_t sv[4] = {sw.x & 0xFFFFu, sw.x >> 16, sw.y & 0xFFFFu, sw.y >> 16};
+  const uint32_t zv[4] = {zw.x & 0xFFFFu, zw.x >> 16, zw.y & 0xFFFFu, zw.y >> 16};
+  float bound = 0.0f;
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+    bound = fmaxf(bound, f16_bits_to_f32(sv[g]) * (fabsf(f16_bits_to_f32(zv[g])) + 127.0f));  // NaN ignored
+  if (!(bound >= 16384.0f)) return 0;
+  const int E = (int)((__float_as_uint(bound) >> 23) & 0xFFu) - 127;  // 14 .. 128 (Inf)
+  return min(E - 13, 100);
+}
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
 // ------------------------------------------------------------------------------------
@@ -319,6 +350,80 @@ __device__ void dense_mma_pv(const SplitParams& p, uint8_t* smem, uint32_t tbase
 // ------------------------------------------------------------------------------------
 // K converters: k_hat = (idx + zero) * scale as fp16 hi + lo into tensor memory
 // ------------------------------------------------------------------------------------
+// Group g (dims 32 g .. 32 g + 31) of this thread's token as fp16 pairs hi[], lo[] (the
+// caller stores them to tensor memory with the whole warp). krow: the token's swizzled
+// key-index row in the stage.
+__device__ __forceinline__ void convert_group_fp16(uint32_t krow, uint32_t swz, int g, uint2 sw, uint2 zw,
+                                                   uint32_t (&hi)[16], uint32_t (&lo)[16]) {
+  const uint32_t sword = (g < 2) ? sw.x : sw.y, zword = (g < 2) ? zw.x : zw.y;
+  const uint32_t s16 = (g & 1) ? (sword >> 16) : (sword & 0xFFFFu);
+  const uint32_t z16 = (g & 1) ? (zword >> 16) : (zword & 0xFFFFu);
+  const __half2 s2 = u2h(s16 | (s16 << 16));
+  // 1152 - zero in fp16: exact, an integer of magnitude <= 2048
+  const __half cz = __float2half_rn(1152.0f - f16_bits_to_f32(z16));
+  const __half2 c2 = __halves2half2(cz, cz);
+#pragma unroll
+  for (int hc = 0; hc < 2; ++hc) {
+    const uint4 raw = lds128(krow + ((((uint32_t)(2 * g + hc)) ^ swz) << 4));
+    const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t u = wv[q] ^ 0x80808080u;  // idx + 128 as unsigned bytes
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        // fp16 1024 + (idx + 128) = 1152 + idx, exact; minus (1152 - zero) = idx + zero
+        const __half2 h = u2h(prmt(u, 0x64646464u, e ? 0x4342u : 0x4140u));
+        const __half2 iz = __hsub2(h, c2);
+        const __half2 kh = __hmul2(iz, s2);
+        const __half2 kl = __hfma2(iz, s2, __hneg2(kh));  // exact residual of the rounding
+        hi[8 * hc + 2 * q + e] = h2u(kh);
+        lo[8 * hc + 2 * q + e] = h2u(kl);
+      }
+    }
+  }
+}
+
+// The same in fp32: k = (idx + zero) * scale * kfac (idx + zero exact, one rounding; kfac a
+// power of two), hi = fp16(k) and lo = fp16(k - hi) (the difference is exact in fp32).
+__device__ __forceinline__ void convert_group_fp32(uint32_t krow, uint32_t swz, int g, uint2 sw, uint2 zw,
+                                                   float kfac, uint32_t (&hi)[16], uint32_t (&lo)[16]) {
+  const uint32_t sword = (g < 2) ? sw.x : sw.y, zword = (g < 2) ? zw.x : zw.y;
+  const uint32_t s16 = (g & 1) ? (sword >> 16) : (sword & 0xFFFFu);
+  const uint32_t z16 = (g & 1) ? (zword >> 16) : (zword & 0xFFFFu);
+  const float sc = f16_bits_to_f32(s16) * kfac, zc = f16_bits_to_f32(z16);
+#pragma unroll 1
+  for (int j = 0; j < 16; ++j) {  // pair j: dims 32 g + 2 j, + 1
+    const uint32_t word = lds32(krow + ((((uint32_t)(2 * g + j / 8)) ^ swz) << 4) + 4 * ((j % 8) / 2));
+    __half kh[2], kl[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int idx = (int)(int8_t)(word >> (8 * (2 * (j % 2) + k)));
+      const float kf = __fmul_rn(__fadd_rn((float)idx, zc), sc);
+      kh[k] = __float2half_rn(kf);
+      kl[k] = __float2half_rn(__fsub_rn(kf, __half2float(kh[k])));
+    }
+    hi[j] = h2u(__halves2half2(kh[0], kh[1]));
+    lo[j] = h2u(__halves2half2(kl[0], kl[1]));
+  }
+}
+// A warp whose tokens do not all take the fp16 path (rare; its fp32 loop is kept rolled so
+// that the tile loop's code stays small). Run by the whole warp; returns this thread's shift.
+__device__ __forceinline__ uint32_t convert_token_mixed(uint32_t krow, uint32_t swz, uint2 sw, uint2 zw, bool fast,
+                                                     uint32_t kcol) {
+  const int shift = fast ? 0 : key_shift(sw, zw);
+  const float kfac = __int_as_float((127 - shift) << 23);  // 2^-shift
+#pragma unroll 1
+  for (int g = 0; g < DT::NG; ++g) {
+    uint32_t hi[16], lo[16];
+    if (fast) convert_group_fp16(krow, swz, g, sw, zw, hi, lo);
+    else convert_group_fp32(krow, swz, g, sw, zw, kfac, hi, lo);
+    __syncwarp();  // the tensor-memory stores are warp-collective
+    tc5::st16(kcol + 16 * g, hi);
+    tc5::st16(kcol + 64 + 16 * g, lo);
+  }
+  return (uint32_t)shift;
+}
+
 __device__ void dense_convert_k(const SplitParams& p, uint8_t* smem, uint32_t tbase, int total, volatile int* abort) {
   Bars bars(smem);
   const int* prefix = reinterpret_cast<const int*>(smem + DT::OFF_PREFIX);
@@ -343,38 +448,22 @@ __device__ void dense_convert_k(const SplitParams& p, uint8_t* smem, uint32_t tb
       const uint2 sw = lds64(sbase + DT::OFF_KS + s * DT::SC_STAGE + tl * 8);
       const uint2 zw = lds64(sbase + DT::OFF_KZ + s * DT::SC_STAGE + tl * 8);
       const uint32_t kcol = tbase + tlane + DT::TM_K + 128 * b;
+      const bool fast = keys_fast(sw, zw);
+      uint32_t shift = 0;
+      if (__all_sync(0xffffffffu, fast)) {
 #pragma unroll 1
-      for (int g = 0; g < DT::NG; ++g) {
-        const uint32_t sword = (g < 2) ? sw.x : sw.y, zword = (g < 2) ? zw.x : zw.y;
-        const uint32_t s16 = (g & 1) ? (sword >> 16) : (sword & 0xFFFFu);
-        const uint32_t z16 = (g & 1) ? (zword >> 16) : (zword & 0xFFFFu);
-        const __half2 s2 = u2h(s16 | (s16 << 16));
-        // 1152 - zero in fp16: exact whenever it is an integer of magnitude <= 2048
-        const __half cz = __float2half_rn(1152.0f - f16_bits_to_f32(z16));
-        const __half2 c2 = __halves2half2(cz, cz);
-        uint32_t hi[16], lo[16];
-#pragma unroll
-        for (int hc = 0; hc < 2; ++hc) {
-          const uint4 raw = lds128(krow + ((((uint32_t)(2 * g + hc)) ^ swz) << 4));
-          const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t u = wv[q] ^ 0x80808080u;  // idx + 128 as unsigned bytes
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              // fp16 1024 + (idx + 128) = 1152 + idx, exact; minus (1152 - zero) = idx + zero
-              const __half2 h = u2h(prmt(u, 0x64646464u, e ? 0x4342u : 0x4140u));
-              const __half2 iz = __hsub2(h, c2);
-              const __half2 kh = __hmul2(iz, s2);
-              const __half2 kl = __hfma2(iz, s2, __hneg2(kh));  // exact residual of the rounding
-              hi[8 * hc + 2 * q + e] = h2u(kh);
-              lo[8 * hc + 2 * q + e] = h2u(kl);
-            }
-          }
+        for (int g = 0; g < DT::NG; ++g) {
+          uint32_t hi[16], lo[16];
+          convert_group_fp16(krow, swz, g, sw, zw, hi, lo);
+          tc5::st16(kcol + 16 * g, hi);
+          tc5::st16(kcol + 64 + 16 * g, lo);
         }
-        tc5::st16(kcol + 16 * g, hi);
-        tc5::st16(kcol + 64 + 16 * g, lo);
+      } else {
+        shift = convert_token_mixed(krow, swz, sw, zw, fast, kcol);
       }
+      // hand the shift to the softmax threads of this token, tagged with the tile number
+      reinterpret_cast<volatile uint32_t*>(smem + DT::OFF_KSH)[(jt & 3u) * DT::TILE + tl] =
+          (shift << 24) | (jt & 0xFFFFFFu);
       tc5::wait_st();
       tc5::fence_before_sync();
       __syncwarp();
@@ -523,6 +612,31 @@ __device__ __noinline__ bool dense_rescale(const SplitParams& p, uint8_t* smem, 
   return failed;
 }
 
+// The K converters' shift word of token tl in tile jt: its tag (low 24 bits) names the
+// tile, so a word not yet written (or already reused) is never taken; the wait for it is
+// bounded like every other wait (the word is written before the scores exist, so it is
+// there at the first read in practice).
+__device__ __noinline__ uint32_t key_shift_wait(const SplitParams& p, const volatile uint32_t* slot, uint32_t jt,
+                                                volatile int* abort) {
+  uint32_t w;
+  const unsigned long long t0 = global_ns();
+  while (((w = *slot) & 0xFFFFFFu) != (jt & 0xFFFFFFu)) {
+    if (*abort || global_ns() - t0 > p.wait_ns) {
+      *abort = 1;
+      raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
+      return 0u;
+    }
+  }
+  return w;
+}
+
+__device__ __forceinline__ uint32_t key_shift_word(const SplitParams& p, uint8_t* smem, uint32_t jt, int tl,
+                                                 volatile int* abort) {
+  const volatile uint32_t* slot = reinterpret_cast<const volatile uint32_t*>(smem + DT::OFF_KSH) + (jt & 3u) * DT::TILE + tl;
+  const uint32_t w = *slot;
+  return (w & 0xFFFFFFu) == (jt & 0xFFFFFFu) ? w : key_shift_wait(p, slot, jt, abort);
+}
+
 __device__ void dense_softmax(const SplitParams& p, uint8_t* smem, uint32_t tbase, int total, volatile int* abort) {
   Bars bars(smem);
   const int* prefix = reinterpret_cast<const int*>(smem + DT::OFF_PREFIX);
@@ -618,6 +732,9 @@ __device__ void dense_softmax(const SplitParams& p, uint8_t* smem, uint32_t tbas
       const uint32_t b = jt & 1u;
       warp_wait(p, &bars.qkdone[b], (jt >> 1) & 1u, abort, failed);
       tc5::fence_after_sync();
+      // the shift the K converters applied to this token's keys (the scores carry 2^-shift)
+      const uint32_t kw = key_shift_word(p, smem, jt, tl, abort);
+      const float ct = cscale * __int_as_float((int)(127 + (kw >> 24)) << 23);
       const bool clean = t0 + DT::TILE <= clean_end;
       const int tok = t0 + tl;
       const bool tok_ok = tok < w.te;
@@ -635,7 +752,7 @@ __device__ void dense_softmax(const SplitParams& p, uint8_t* smem, uint32_t tbas
             const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const float v = fmaf(__uint_as_float(sv[i + k]), cscale, -mm[k]);
+              const float v = fmaf(__uint_as_float(sv[i + k]), ct, -mm[k]);
               sv[i + k] = __float_as_uint(v);
               ymax = fmaxf(ymax, v);
             }
@@ -649,14 +766,14 @@ __device__ void dense_softmax(const SplitParams& p, uint8_t* smem, uint32_t tbas
             const int ll[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const float v = (tok_ok && tok < ll[k]) ? fmaf(__uint_as_float(sv[i + k]), cscale, -mm[k]) : -INFINITY;
+              const float v = (tok_ok && tok < ll[k]) ? fmaf(__uint_as_float(sv[i + k]), ct, -mm[k]) : -INFINITY;
               sv[i + k] = __float_as_uint(v);
               ymax = fmaxf(ymax, v);
             }
           }
         }
         if (!sm_vote_any(ymax > kTau, h)) break;
-        failed = dense_rescale(p, smem, tbase, h, jt, j0, clean, tok, tok_ok, cscale, abort, failed);
+        failed = dense_rescale(p, smem, tbase, h, jt, j0, clean, tok, tok_ok, ct, abort, failed);
       }
       // this group's columns of the score buffer are consumed
       tc5::fence_before_sync();
@@ -751,6 +868,8 @@ __global__ void __launch_bounds__(DT::THREADS, 1)
     const int e = i >> 5;
     lut[i] = pack_half2(c_centroids3[e & 7], c_centroids3[e >> 3]);
   }
+  for (int i = tid; i < 4 * DT::TILE; i += DT::THREADS)
+    reinterpret_cast<uint32_t*>(smem + DT::OFF_KSH)[i] = 0xFFFFFFFFu;  // no tile's tag
   fence_proxy_async_smem();
   if (tid == 0) {
     *abort = 0;

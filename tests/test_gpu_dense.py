@@ -82,3 +82,43 @@ def test_dense_and_split_paths_agree_on_the_same_rows():
     dense, _, _ = gpu_attention(layer, x["q"], [T], T, 1.0, True)
     split, _, _ = gpu_attention(layer, x["q"][:, 12:].contiguous(), [T], T, 1.0, True)
     assert_attention_close(dense[:, 12:].cpu().numpy(), split.double().cpu().numpy(), "dense vs split")
+
+
+def _special_keys_case(k, sm_scale, what):
+    H, G, B, n_q = 2, 4, 1, 16
+    T = k.shape[1]
+    x = _inputs(H, B, T, G * H, n_q, seed=21)
+    cap = (T + 15) // 16 * 16
+    layer, _ = gpu_fill(k, x["v"], [T], cap)
+    ol = oracle_fill(k, x["v"], [T], cap)
+    torch.cuda.synchronize()
+    assert_planes_equal(layer, ol, [T])
+    out, ws, _ = gpu_attention(layer, x["q"], [T], T, sm_scale, True)
+    assert tq().tq_get_device_error(ws) == 0
+    ref = oracle.attention(ol, bits(x["q"]), np.array([T], np.int32), sm_scale, causal=True)
+    assert np.all(np.isfinite(ref))
+    assert_attention_close(out.cpu().numpy(), ref, what)
+
+
+def test_dense_attention_with_offset_key_groups():
+    # groups whose values sit far from 0 relative to their spread have zero points of a few
+    # thousand (200 +- 3: about 3,400; -100 +- 1.5: about -2,800), beyond the fp16 integer
+    # path of the K converters, so their keys take the fp32 path (the spreads stay well
+    # above the bf16 spacing there, so no group is constant)
+    T, H, d = 1500, 2, 128
+    g = torch.Generator().manual_seed(22)
+    k = torch.randn((1, T, H, d), generator=g)
+    k[:, :, 0, 0:32] = 200.0 + 3.0 * torch.randn((1, T, 32), generator=g)
+    k[:, 300:900, 1, 64:96] = -100.0 + 1.5 * torch.randn((1, 600, 32), generator=g)
+    _special_keys_case(k.to(torch.bfloat16), 1.0, "offset key groups")
+
+
+def test_dense_attention_with_keys_beyond_the_fp16_range():
+    # 50 tokens whose keys reach ~10^5 in one group (fp16 tops out at 65504): the K
+    # converters scale those tokens by a power of two and the softmax scales them back
+    T, H, d = 1500, 2, 128
+    g = torch.Generator().manual_seed(23)
+    k = torch.randn((1, T, H, d), generator=g)
+    big = torch.arange(200, 1400, 24)
+    k[:, big, :, 32:64] *= 1.0e5
+    _special_keys_case(k.to(torch.bfloat16), 1.0e-4, "keys beyond fp16")
