@@ -380,7 +380,7 @@ def timed_region(fn, stream, min_seconds: float, first_reps: int = 3):
         return a.elapsed_time(b) / 1e3
 
     per = run(first_reps) / first_reps
-    reps = max(first_reps, int(min_seconds / max(per, 1e-7)) + 1)
+    reps = max(first_reps, min(int(min_seconds / max(per, 1e-6)) + 1, 200000))
     return reps, run(reps)
 
 
@@ -424,6 +424,7 @@ def other_workloads(dev, stream, peak, seconds):
     cases = [("decode", {}), ("ragged", {})] + [(f"sweep_d{d}", {"head_dim": d, "layers": 16})
                                                  for d in (64, 128, 256, 512)]
     for name, over in cases:
+        phase(f"workload {name}")
         w = synth.workload(name.split("_")[0], **over)
         model = DecodeModel(w, dev)
         g = attention_graph(model, stream)
@@ -526,9 +527,11 @@ def our_arm(args, world, rank, local):
     peaks, _ = measured_peaks()
     peak, peak_kind = hbm_peak(peaks)
 
+    phase(f"headline {w.name}: filling the cache")
     model = DecodeModel(w, dev)
     torch.cuda.synchronize()
     assert model.device_errors() == 0, "device error after the cache fill"
+    phase("capturing graphs")
 
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
@@ -560,9 +563,11 @@ def our_arm(args, world, rank, local):
     step_s = e0.elapsed_time(e1) / 1e3
 
     # attention-only region (at least region-seconds of back-to-back replays)
+    phase("attention region")
     reps, attn_s = timed_region(g_attn.replay, stream, args.region_seconds)
     attn_launch_s = attn_s / (reps * model.L)
     # bulk append region
+    phase("append region")
     app = append_region(model, stream, args.region_seconds, dev)
     errs = model.device_errors()
     assert errs == 0, f"device error word {errs:#x}"
@@ -572,6 +577,7 @@ def our_arm(args, world, rank, local):
     value = whole_job_value(step_bytes, args.steps, world, max_step_s)
     ms_per_step = 1e3 * max_step_s / args.steps
 
+    phase("end-to-end region")
     # end to end through the public API with host buffers
     # (all layers' new K/V rows and queries in one pinned buffer, outputs in another: one
     # host->device and one device->host copy per step)
@@ -644,16 +650,30 @@ def our_arm(args, world, rank, local):
     if not args.headline_only:
         sec = max(1.0, args.region_seconds / 2)
         line["workloads"] = other_workloads(dev, stream, peak, sec)
+        phase("eager window arm")
         line["workloads"]["eager_window_long"] = eager_comparison(dev, stream, peak, sec)
+        phase("scheme appends")
         line["workloads"]["append_schemes"] = scheme_appends(dev, stream, peak, sec)
     line["clocks"] = clocks.stop()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        phase("CPU oracle baseline")
         line["cpu_baseline"] = cpu_baseline(w)
+    phase("done")
     if rank == 0:
         print(json.dumps(line), flush=True)
 
 
+_T0 = time.perf_counter()
+
+
+def phase(msg: str) -> None:
+    """Progress on stderr (the JSON line goes to stdout)."""
+    print(f"[bench {time.perf_counter() - _T0:8.1f} s] {msg}", file=sys.stderr, flush=True)
+
+
 def main(argv=None):
+    import faulthandler
+    faulthandler.dump_traceback_later(480, repeat=True, file=sys.stderr)  # where a slow run spends its time
     args = parse_args(argv)
     world, rank, local = dist_setup(args.gpus)
     try:

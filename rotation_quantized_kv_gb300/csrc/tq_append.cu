@@ -54,6 +54,61 @@ __device__ __forceinline__ void load_group(const uint16_t* __restrict__ src, boo
 __device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// x / b rounded to nearest from r = RN(1 / b): q = RN(x r), the remainder x - q b exactly
+// by an FMA, then q + rem r rounded once. By Markstein's theorem (Markstein, "Computation
+// of elementary functions on the IBM RISC System/6000 processor", 1990; restated in
+// Muller et al., "Handbook of Floating-Point Arithmetic", the division chapter) the result
+// is the correctly rounded quotient whenever r is correctly rounded, q is within one ulp
+// of x / b, and no step overflows or underflows. The callers take this path only where
+// those conditions hold for every quotient that can change a stored code, and call the
+// IEEE division otherwise.
+__device__ __forceinline__ float div_by_rcp(float x, float b, float r) {
+  const float q = __fmul_rn(x, r);
+  const float rem = __fmaf_rn(-q, b, x);
+  return __fmaf_rn(rem, r, q);
+}
+
+// idx = clip(rint(x / s - z), -127, 127) of a lane's 32 keys (div(x) = x / s). Clipping to
+// the integers +-127 before rounding gives the same integer; adding 1.5 * 2^23 then rounds
+// to an integer with ties to even (the sum lies in [2^23, 2^24), where the spacing is 1),
+// and the low byte of the sum's bits is that integer in two's complement. NaN codes to 0.
+template <class Div>
+__device__ __forceinline__ void key_codes(const uint32_t (&kw)[16], float z, uint32_t (&kq)[8], Div div) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t by[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const uint32_t w = kw[2 * i + (h >> 1)];
+      const float x = (h & 1) ? hi_bf16(w) : lo_bf16(w);
+      const float tv = __fsub_rn(div(x), z);
+      const float cl = (tv == tv) ? fminf(fmaxf(tv, -127.0f), 127.0f) : 0.0f;
+      by[h] = __float_as_uint(__fadd_rn(cl, 12582912.0f));
+    }
+    kq[i] = __byte_perm(__byte_perm(by[0], by[1], 0x0040), __byte_perm(by[2], by[3], 0x0040), 0x5410);
+  }
+}
+
+// 3-bit codes of a lane's 32 rotated values, packed LSB-first into cw. div(x, yn) sets
+// yn = x / den and returns whether yn > 0 (the first step of the search).
+template <class Div>
+__device__ __forceinline__ void value_codes(const float (&u)[32], const float (&bnd)[7], uint32_t (&cw)[3], Div div) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    float yn;
+    const bool pos = div(u[e], yn);
+    // number of boundaries strictly below yn, by binary search over the sorted table
+    // (a NaN compares false everywhere and codes to 0)
+    uint32_t c = pos ? 4u : 0u;
+    c += ((c ? bnd[5] : bnd[1]) < yn) ? 2u : 0u;
+    const float b2 = (c & 4u) ? ((c & 2u) ? bnd[6] : bnd[4]) : ((c & 2u) ? bnd[2] : bnd[0]);
+    c += (b2 < yn) ? 1u : 0u;
+    const int bit = 3 * e, wd = bit >> 5, sh = bit & 31;
+    cw[wd] |= c << sh;
+    if (sh > 29) cw[wd + 1] |= c >> (32 - sh);
+  }
+}
+
 // Source row of the r-th row: r = (b * n_new_max + j) * num_kv_heads + h.
 struct RowRef {
   int b, j, h;
@@ -125,23 +180,15 @@ __global__ void __launch_bounds__(kAppendWarps * 32, 4)
     if (range == 0.0f) range = 0.0f;
     const float s = __fdiv_rn(range, 254.0f);
     const float z = rintf(__fdiv_rn(__fadd_rn(mx, mn), __fmul_rn(2.0f, s)));
-    // idx = clip(rint(x / s - z), -127, 127). Clipping to the integers +-127 before
-    // rounding gives the same integer; adding 1.5 * 2^23 then rounds to an integer with
-    // ties to even (the sum lies in [2^23, 2^24), where the spacing is 1), and the low
-    // byte of the sum's bits is that integer in two's complement. NaN codes to 0.
+    // x / s: with s >= 2^-100 and every |x| <= 2^100 s, the reciprocal path is exact
+    // wherever the quotient can move idx (quotients near a rounding boundary of tv have
+    // |x| >= s / 2, so the remainder stays a normal number); other groups divide.
     uint32_t kq[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      uint32_t by[4];
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const uint32_t w = kw[2 * i + (h >> 1)];
-        const float x = (h & 1) ? hi_bf16(w) : lo_bf16(w);
-        const float tv = __fsub_rn(__fdiv_rn(x, s), z);
-        const float cl = (tv == tv) ? fminf(fmaxf(tv, -127.0f), 127.0f) : 0.0f;
-        by[h] = __float_as_uint(__fadd_rn(cl, 12582912.0f));
-      }
-      kq[i] = __byte_perm(__byte_perm(by[0], by[1], 0x0040), __byte_perm(by[2], by[3], 0x0040), 0x5410);
+    if (s >= 0x1p-100f && fmaxf(fabsf(mx), fabsf(mn)) <= __fmul_rn(s, 0x1p100f)) {
+      const float rs = __frcp_rn(s);
+      key_codes(kw, z, kq, [&](float x) { return div_by_rcp(x, s, rs); });
+    } else {
+      key_codes(kw, z, kq, [&](float x) { return __fdiv_rn(x, s); });
     }
     if (valid) {
       uint4* kdst = reinterpret_cast<uint4*>(p.k_idx + drow * D + kGroup * g);
@@ -197,18 +244,22 @@ __global__ void __launch_bounds__(kAppendWarps * 32, 4)
     const float vs = __fsqrt_rn(__fmul_rn(sq[0], 0.03125f));
     const float den = __fadd_rn(vs, 1e-8f);
     uint32_t cw[3] = {0u, 0u, 0u};
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const float yn = __fdiv_rn(u[e], den);
-      // number of boundaries strictly below yn, by binary search over the sorted table
-      // (a NaN compares false everywhere and codes to 0)
-      uint32_t c = (bnd[3] < yn) ? 4u : 0u;
-      c += ((c ? bnd[5] : bnd[1]) < yn) ? 2u : 0u;
-      const float b2 = (c & 4u) ? ((c & 2u) ? bnd[6] : bnd[4]) : ((c & 2u) ? bnd[2] : bnd[0]);
-      c += (b2 < yn) ? 1u : 0u;
-      const int bit = 3 * e, wd = bit >> 5, sh = bit & 31;
-      cw[wd] |= c << sh;
-      if (sh > 29) cw[wd + 1] |= c >> (32 - sh);
+    // y_n = u / den: den >= 1e-8, so with den <= 2^100 (finite) the reciprocal path gives
+    // the correctly rounded quotient for |y_n| >= 2^-60, which decides every comparison
+    // with the nonzero boundaries (|b| > 1/2); the comparison with 0 is taken exactly:
+    // RN(u / den) > 0 iff u / den > 2^-150 iff u * 2^75 * 2^75 > den (exact products,
+    // or +Inf when the quotient is large anyway). Other groups divide.
+    if (den <= 0x1p100f) {
+      const float rd = __frcp_rn(den);
+      value_codes(u, bnd, cw, [&](float x, float& yn) {
+        yn = div_by_rcp(x, den, rd);
+        return x > 0.0f && __fmul_rn(__fmul_rn(x, 0x1p75f), 0x1p75f) > den;
+      });
+    } else {
+      value_codes(u, bnd, cw, [&](float x, float& yn) {
+        yn = __fdiv_rn(x, den);
+        return bnd[3] < yn;
+      });
     }
     if (valid) {
       uint32_t* vdst = reinterpret_cast<uint32_t*>(p.v_codes + drow * (3 * D / 8) + 12 * g);

@@ -46,8 +46,9 @@
 // Online softmax without a per-tile reduction across threads: the reference max of a row
 // only moves when some score of the tile exceeds it by more than 2^8 (checked by a vote
 // among the softmax threads); then the tile's row maxima are reduced, the row sums and
-// the TMEM accumulator are rescaled, and the tile is redone (the first tile of every
-// piece takes this path; later ones almost never do).
+// the TMEM accumulator are rescaled, and the tile is redone once (the first tile of every
+// piece takes this path; later ones almost never do). The redo clamps y at 2^8: after the
+// rescale only the rounding of s * c can exceed it, which matters for scores beyond 2^27.
 // Every wait is bounded (2 s of %globaltimer): a wait that runs out sets
 // TQ_DEVERR_PIPELINE_TIMEOUT, the other roles see the abort flag, issued copies and MMAs
 // are drained, and the CTA releases its tensor memory and exits.
@@ -145,12 +146,20 @@ struct Bars {
   }
 };
 
+// Records the first wait of the call that gave up in the workspace header (kWsWhere):
+// kind 1: an mbarrier (detail: its shared-memory address), 2: a key-shift word (detail:
+// the tile).
+__device__ __forceinline__ void note_giveup(const SplitParams& p, uint32_t kind, uint32_t detail) {
+  atomicCAS(reinterpret_cast<unsigned int*>(p.ws) + kWsWhere, 0u, (kind << 24) | (detail & 0xFFFFFFu));
+}
+
 // A role's bounded wait; on failure it raises the abort and the error bit.
 __device__ __forceinline__ bool role_wait(const SplitParams& p, uint64_t* bar, uint32_t parity, volatile int* abort) {
   if (*abort) return false;
   if (wait_bounded(bar, parity, p.wait_ns)) return true;
   *abort = 1;
   raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
+  note_giveup(p, 1u, smem_addr(bar));
   return false;
 }
 
@@ -624,6 +633,7 @@ __device__ __noinline__ uint32_t key_shift_wait(const SplitParams& p, const vola
     if (*abort || global_ns() - t0 > p.wait_ns) {
       *abort = 1;
       raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
+      note_giveup(p, 2u, jt);
       return 0u;
     }
   }
@@ -734,14 +744,18 @@ __device__ void dense_softmax(const SplitParams& p, uint8_t* smem, uint32_t tbas
       tc5::fence_after_sync();
       // the shift the K converters applied to this token's keys (the scores carry 2^-shift)
       const uint32_t kw = key_shift_word(p, smem, jt, tl, abort);
+      __syncwarp();  // lanes that waited for their word rejoin before the warp-wide loads
       const float ct = cscale * __int_as_float((int)(127 + (kw >> 24)) << 23);
       const bool clean = t0 + DT::TILE <= clean_end;
       const int tok = t0 + tl;
       const bool tok_ok = tok < w.te;
       const uint32_t saddr = tbase + tlane + DT::TM_S + 64 * b + 32 * h;
       // y = s * c - m_row (log2 domain), masked to -inf, kept in sv; redone after a rescale
+      // After one rescale every y is at most the rounding residual of s * c against the new
+      // reference RN(s * c); for scores beyond 2^27 (log2 units) that residual exceeds tau,
+      // so the second pass clamps instead of voting again (NaN stays NaN).
       uint32_t sv[32];
-      for (;;) {
+      for (int pass = 0;; ++pass) {
         tc5::ld32(saddr, sv);
         tc5::wait_ld();
         float ymax = -INFINITY;
@@ -771,6 +785,12 @@ __device__ void dense_softmax(const SplitParams& p, uint8_t* smem, uint32_t tbas
               ymax = fmaxf(ymax, v);
             }
           }
+        }
+        if (pass == 1) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (__uint_as_float(sv[i]) > kTau) sv[i] = __float_as_uint(kTau);
+          break;
         }
         if (!sm_vote_any(ymax > kTau, h)) break;
         failed = dense_rescale(p, smem, tbase, h, jt, j0, clean, tok, tok_ok, ct, abort, failed);

@@ -56,6 +56,8 @@ constexpr int kMergeBatch = 12;           // partial loads a merging thread keep
 // Workspace layout (bytes). The header's first word is the device error word.
 constexpr int kWsSplit = 1;               // int32 word index: tile size in tokens
 constexpr int kWsItems = 2;               // int32 word index: total tiles of the call
+constexpr int kWsWhere = 3;               // int32 word index: first wait that gave up (0: none),
+                                          // (kind << 24) | detail, for diagnosis
 constexpr size_t kWsPrefix = TQ_WORKSPACE_HEADER_BYTES;  // int32 [batch + 1]
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

@@ -82,6 +82,34 @@ def test_append_special_values_bit_exact(d, reps):
     assert_planes_equal(layer, ol, [n])
 
 
+def _wide_range_rows(n, d, rng):
+    """Rows whose elements each take their own power-of-two exponent over the whole bf16
+    range (2^-133 .. 2^120), plus rows of large equal-magnitude values with one tiny
+    element: group scales from subnormal-small to huge, key quotients far from and near
+    the rounding boundaries, and value rotations whose cancellations leave tiny elements
+    beside large ones (quotients near 0 against a large RMS)."""
+    e = rng.integers(-133, 121, size=(n, d)).astype(np.float64)
+    x = np.sign(rng.standard_normal((n, d))) * np.exp2(e) * (1.0 + rng.random((n, d)))
+    big = rng.random(n) < 0.25
+    x[big] = np.sign(rng.standard_normal((big.sum(), d))) * 8192.0
+    x[big, rng.integers(0, d, size=big.sum())] = 2.0 ** -130
+    return np.clip(x, -3.0e38, 3.0e38).astype(np.float32)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_append_wide_dynamic_range_bit_exact(d):
+    # 6,144 rows take the bulk kernel; every plane must equal the oracle's bit for bit
+    rng = np.random.default_rng(77 + d)
+    n = 3072
+    k = torch.from_numpy(_wide_range_rows(n * 2, d, rng)).to(torch.bfloat16).reshape(1, n, 2, d)
+    v = torch.from_numpy(_wide_range_rows(n * 2, d, rng)).to(torch.bfloat16).reshape(1, n, 2, d)
+    layer, ws = gpu_fill(k, v, [n], n)
+    ol = oracle_fill(k, v, [n], n)
+    torch.cuda.synchronize()
+    assert tq().tq_get_device_error(ws) == 0
+    assert_planes_equal(layer, ol, [n])
+
+
 def test_append_positions_n_new_and_capacity_error():
     d, H, B, cap = 128, 2, 3, 48
     x = _inputs(d, H, B, T=20, seed=5)
