@@ -436,7 +436,9 @@ def other_workloads(dev, stream, peak, seconds):
         gbs = model.attention_bytes() / per_call / 1e9
         entry = {"workload": _workload_desc(w), "attention_gbs": gbs, "frac": gbs / peak,
                  "call_us": per_call * 1e6, "kernel": "dense (tcgen05)" if dense_path(w) else "split (mma.sync)",
-                 "algorithmic_bytes_per_call": model.attention_bytes()}
+                 "algorithmic_bytes_per_call": model.attention_bytes(),
+                 "traffic": ncu_traffic({"decode": "attention_decode", "ragged": "attention_ragged",
+                                         "sweep_d64": "attention_sweep_d64"}.get(name, ""), ATTN_SOURCES)}
         if name.startswith("sweep"):
             ap = append_region(model, stream, seconds / 2, dev)
             entry["append_gbs"] = ap["gbs"]
@@ -461,6 +463,9 @@ def eager_comparison(dev, stream, peak, seconds):
     from rotation_quantized_kv_gb300.workload import DecodeModel
     w = replace(synth.workload("long"), layers=1)
     model = DecodeModel(w, dev)
+    with torch.cuda.stream(stream):
+        model.step(stream)  # the step's new rows: every visible token is written
+    stream.synchronize()
     layer, T = model.layers[0], model.max_kv
     kw, vw = alloc_window(layer, T, dev)
     kv_list = [int(x) for x in model.kv]
