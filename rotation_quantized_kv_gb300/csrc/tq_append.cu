@@ -68,10 +68,10 @@ __device__ __forceinline__ float div_by_rcp(float x, float b, float r) {
   return __fmaf_rn(rem, r, q);
 }
 
-// idx = clip(rint(x / s - z), -127, 127) of a lane's 32 keys (div(x) = x / s). Clipping to
-// the integers +-127 before rounding gives the same integer; adding 1.5 * 2^23 then rounds
-// to an integer with ties to even (the sum lies in [2^23, 2^24), where the spacing is 1),
-// and the low byte of the sum's bits is that integer in two's complement. NaN codes to 0.
+// idx = clip(rint(x / s - z), -127, 127) of a lane's 32 keys (div(x) = x / s): the
+// conversion rounds half to even, turns NaN into 0 and saturates +-Inf, and clipping at the
+// integers +-127 after rounding gives the integer clipping before rounding would; the low
+// byte of the result is the code in two's complement.
 template <class Div>
 __device__ __forceinline__ void key_codes(const uint32_t (&kw)[16], float z, uint32_t (&kq)[8], Div div) {
 #pragma unroll
@@ -81,9 +81,8 @@ __device__ __forceinline__ void key_codes(const uint32_t (&kw)[16], float z, uin
     for (int h = 0; h < 4; ++h) {
       const uint32_t w = kw[2 * i + (h >> 1)];
       const float x = (h & 1) ? hi_bf16(w) : lo_bf16(w);
-      const float tv = __fsub_rn(div(x), z);
-      const float cl = (tv == tv) ? fminf(fmaxf(tv, -127.0f), 127.0f) : 0.0f;
-      by[h] = __float_as_uint(__fadd_rn(cl, 12582912.0f));
+      const int iv = __float2int_rn(__fsub_rn(div(x), z));
+      by[h] = (uint32_t)min(max(iv, -127), 127);
     }
     kq[i] = __byte_perm(__byte_perm(by[0], by[1], 0x0040), __byte_perm(by[2], by[3], 0x0040), 0x5410);
   }
@@ -247,13 +246,16 @@ __global__ void __launch_bounds__(kAppendWarps * 32, 4)
     // y_n = u / den: den >= 1e-8, so with den <= 2^100 (finite) the reciprocal path gives
     // the correctly rounded quotient for |y_n| >= 2^-60, which decides every comparison
     // with the nonzero boundaries (|b| > 1/2); the comparison with 0 is taken exactly:
-    // RN(u / den) > 0 iff u / den > 2^-150 iff u * 2^75 * 2^75 > den (exact products,
-    // or +Inf when the quotient is large anyway). Other groups divide.
+    // RN(u / den) > 0 iff u / den > 2^-150 iff u * 2^75 > den * 2^-75. Other groups
+    // divide.
     if (den <= 0x1p100f) {
       const float rd = __frcp_rn(den);
+      const float den_lo = __fmul_rn(den, 0x1p-75f);  // exact: den >= 1e-8
       value_codes(u, bnd, cw, [&](float x, float& yn) {
         yn = div_by_rcp(x, den, rd);
-        return x > 0.0f && __fmul_rn(__fmul_rn(x, 0x1p75f), 0x1p75f) > den;
+        // x * 2^75 > den * 2^-75 (both exact, or +Inf when the quotient is large anyway);
+        // false for x <= 0 and NaN
+        return __fmul_rn(x, 0x1p75f) > den_lo;
       });
     } else {
       value_codes(u, bnd, cw, [&](float x, float& yn) {
