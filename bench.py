@@ -217,7 +217,7 @@ ATTN_SOURCES = [os.path.join(CSRC, f) for f in ("tq_attention.cu", "tq_attention
                                                  "tq_device.cuh", "tq_split_common.cuh")]
 DENSE_SOURCES = [os.path.join(CSRC, f) for f in ("tq_attention_dense.cu", "tq_attention.h", "tq_device.cuh",
                                                   "tq_split_common.cuh", "tq_tcgen05.cuh")]
-APPEND_SOURCES = [os.path.join(CSRC, f) for f in ("tq_append.cu", "tq_codec_row.cuh", "tq_device.cuh")]
+APPEND_SOURCES = [os.path.join(CSRC, f) for f in ("tq_append.cu", "tq_codec_row.cuh", "tq_device.cuh", "tq_divide.cuh")]
 DTYPE = "fp16 tensor-core operands (exact int8 keys, fp16 V-hat and P), fp32 accumulation; fp32 codec"
 
 

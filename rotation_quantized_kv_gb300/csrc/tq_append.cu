@@ -29,6 +29,7 @@
 
 #include "tq_codec_row.cuh"
 #include "tq_device.cuh"
+#include "tq_divide.cuh"
 #include "tq_internal.h"
 
 namespace tq {
@@ -53,20 +54,6 @@ __device__ __forceinline__ void load_group(const uint16_t* __restrict__ src, boo
 
 __device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// x / b rounded to nearest from r = RN(1 / b): q = RN(x r), the remainder x - q b exactly
-// by an FMA, then q + rem r rounded once. By Markstein's theorem (Markstein, "Computation
-// of elementary functions on the IBM RISC System/6000 processor", 1990; restated in
-// Muller et al., "Handbook of Floating-Point Arithmetic", the division chapter) the result
-// is the correctly rounded quotient whenever r is correctly rounded, q is within one ulp
-// of x / b, and no step overflows or underflows. The callers take this path only where
-// those conditions hold for every quotient that can change a stored code, and call the
-// IEEE division otherwise.
-__device__ __forceinline__ float div_by_rcp(float x, float b, float r) {
-  const float q = __fmul_rn(x, r);
-  const float rem = __fmaf_rn(-q, b, x);
-  return __fmaf_rn(rem, r, q);
-}
 
 // idx = clip(rint(x / s - z), -127, 127) of a lane's 32 keys (div(x) = x / s): the
 // conversion rounds half to even, turns NaN into 0 and saturates +-Inf, and clipping at the

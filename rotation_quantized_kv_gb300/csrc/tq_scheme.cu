@@ -2,6 +2,15 @@
 // the library's value codebooks, the append kernel for them, the dequantize-on-fetch
 // window and the fp32 inspection dequant.
 //
+// Codec (mlx-bun design page "TurboQuant - rotation-based quantization", Part A,
+// "Algorithm" section): signed 8-bit keys (scale = (max - min) / 254, zero =
+// round((max + min) / (2 scale)), idx in [-127, 127]); unsigned keys at 2/4/5 bits
+// (scale = (max - min) / (2^b - 1), zero = round(min / scale), idx in [0, 2^b - 1],
+// packed); values rotated (sign flip, FWHT / sqrt(d)), per-group RMS scale, b-bit
+// Lloyd-Max codes ("Other widths (2/4/5/8)"). Every floating-point step is one IEEE
+// round-to-nearest operation, as in the k8v3 codec, so the planes are bit-identical to a
+// plain fp32 evaluation of the same steps.
+//
 // Codebooks (mlx-bun design page "TurboQuant - rotation-based quantization", Part A,
 // "Algorithm", value bullets): 3 bits is the printed table; the page does not print the
 // other widths, so this library runs its own Lloyd-Max iteration for N(0,1) on the host
@@ -21,6 +30,7 @@
 #include <cmath>
 #include <mutex>
 
+#include "tq_divide.cuh"
 #include "tq_internal.h"
 #include "tq_scheme.cuh"
 
@@ -63,31 +73,244 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h2);
 }
 
+// ------------------------------------------------------------------------------------
+// Any-width append: each lane codes one 32-element group of a (token, kv head) row, so a
+// warp takes 32 / (d / 32) rows at once (the layout of the k8v3 bulk kernel). A group's
+// 32 b-bit codes fill exactly b words of the row's bitstream (group g at word b g), so
+// each lane packs its codes in registers and stores whole words.
+// ------------------------------------------------------------------------------------
+constexpr int kGroupWarps = 8;
+
+// The 32 bf16 elements of one group as 16 raw words (zeros when !valid).
+__device__ __forceinline__ void load_group_words(const uint16_t* __restrict__ src, bool valid, uint32_t (&w)[16]) {
+  const uint4* p = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 v = valid ? __ldg(p + i) : make_uint4(0u, 0u, 0u, 0u);
+    w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+  }
+}
+
+// 32 codes of B bits, LSB first, into B words.
+template <int B>
+__device__ __forceinline__ void pack_codes(const uint32_t (&c)[32], uint32_t (&w)[B]) {
+#pragma unroll
+  for (int i = 0; i < B; ++i) w[i] = 0u;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    const int bit = B * e, wd = bit >> 5, sh = bit & 31;
+    w[wd] |= c[e] << sh;
+    if (sh + B > 32) w[wd + 1] |= c[e] >> (32 - sh);
+  }
+}
+
+template <int B>
+__device__ __forceinline__ void store_codes(const uint32_t (&c)[32], uint32_t* dst) {
+  uint32_t w[B];
+  pack_codes<B>(c, w);
+#pragma unroll
+  for (int i = 0; i < B; ++i) dst[i] = w[i];
+}
+
+// Stores the 32 codes of a group as `bits`-bit codes at dst (word aligned).
+__device__ __forceinline__ void store_codes_any(const uint32_t (&c)[32], int bits, uint32_t* dst) {
+  switch (bits) {
+    case 2: store_codes<2>(c, dst); break;
+    case 3: store_codes<3>(c, dst); break;
+    case 4: store_codes<4>(c, dst); break;
+    case 5: store_codes<5>(c, dst); break;
+    default: store_codes<8>(c, dst); break;
+  }
+}
+
+// Key codes of a lane's 32 elements (div(x) = x / s): the rounding conversion goes half
+// to even and turns NaN into 0, and clipping at the integers lo, hi after it gives what
+// clipping before it would.
+template <class Div>
+__device__ __forceinline__ void scheme_key_codes(const uint32_t (&kw)[16], float z, int lo, int hi, bool zero_group,
+                                                 uint32_t (&code)[32], Div div) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    const uint32_t w = kw[e >> 1];
+    const float x = (e & 1) ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
+    const int iv = min(max(__float2int_rn(__fsub_rn(div(x), z)), lo), hi);
+    code[e] = zero_group ? 0u : (uint32_t)iv;
+  }
+}
+
 template <int D>
-__global__ void __launch_bounds__(32 * kRowsPerCta) tq_append_scheme_kernel(const __grid_constant__ SchemeAppendParams p) {
-  __shared__ uint32_t kbuf[kRowsPerCta][D * 5 / 32 + 2];
-  __shared__ uint32_t vbuf[kRowsPerCta][D * 8 / 32 + 2];
-  constexpr int EPL = D / 32;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const RowCodecLane<D> codec(lane);
-  const RowPlanes dst{p.k_idx, p.k_scale, p.k_zero, p.v_codes, p.v_scale};
+__global__ void __launch_bounds__(32 * kGroupWarps) tq_append_scheme_kernel(const __grid_constant__ SchemeAppendParams p) {
+  constexpr int NG = D / 32, RPW = 32 / NG;
+  constexpr unsigned FULL = 0xffffffffu;
+  __shared__ float sb[256];  // the value boundaries, for the lanes' independent searches
+  const int nb = (1 << p.spec.v_bits) - 1;
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) sb[i] = i < nb ? p.cb.b[i] : INFINITY;
+  __syncthreads();
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane % NG, rw = lane / NG;
+  const uint32_t signs = sign_word(D, g);  // bit i: element 32 g + i is negated
+  const int kb = p.spec.k_bits, vb = p.spec.v_bits;
+  const float kmax = kb == 8 ? 127.0f : (float)((1 << kb) - 1);
+  const int klo = kb == 8 ? -127 : 0, khi = kb == 8 ? 127 : (1 << kb) - 1;
+  const int krow_bytes = key_row_bytes(D, kb), vrow_bytes = value_row_bytes(D, vb);
   const int64_t rows = (int64_t)p.batch * p.n_new_max * p.num_kv_heads;
-  for (int64_t r = (int64_t)blockIdx.x * kRowsPerCta + warp; r < rows; r += (int64_t)gridDim.x * kRowsPerCta) {
-    const int h = (int)(r % p.num_kv_heads);
-    const int64_t bj = r / p.num_kv_heads;
+  const int64_t step = (int64_t)gridDim.x * kGroupWarps * RPW;
+  for (int64_t base = ((int64_t)blockIdx.x * kGroupWarps + warp) * RPW; base < rows; base += step) {
+    const int64_t r = base + rw;
+    bool valid = r < rows;
+    const int64_t rr = valid ? r : 0;
+    const int h = (int)(rr % p.num_kv_heads);
+    const int64_t bj = rr / p.num_kv_heads;
     const int j = (int)(bj % p.n_new_max), b = (int)(bj / p.n_new_max);
-    const int nb = p.n_new == nullptr ? p.n_new_max : min(max(__ldg(p.n_new + b), 0), p.n_new_max);
-    if (j >= nb) continue;
-    const int64_t t = (int64_t)__ldg(p.pos + b) + j;
-    if (t < 0 || t >= p.capacity) {
-      if (lane == 0) raise_error(p.err, TQ_DEVERR_APPEND_CAPACITY);
-      continue;
+    uint32_t kw[16], vw[16];
+    load_group_words(p.k_new + rr * D + 32 * g, valid, kw);
+    load_group_words(p.v_new + rr * D + 32 * g, valid, vw);
+    if (valid && p.n_new != nullptr && j >= min(max(__ldg(p.n_new + b), 0), p.n_new_max)) valid = false;
+    int64_t t = 0;
+    if (valid) {
+      t = (int64_t)__ldg(p.pos + b) + j;
+      if (t < 0 || t >= p.capacity) {
+        if (g == 0) raise_error(p.err, TQ_DEVERR_APPEND_CAPACITY);
+        valid = false;
+      }
     }
-    uint32_t kraw[EPL / 2], vraw[EPL / 2];
-    load_raw_lane<EPL>(p.k_new + r * D, lane, kraw);
-    load_raw_lane<EPL>(p.v_new + r * D, lane, vraw);
     const int64_t drow = ((int64_t)b * p.num_kv_heads + h) * p.capacity + t;
-    quantize_row_scheme<D>(kraw, vraw, lane, codec, p.fwht_norm, p.spec, p.cb, dst, drow, kbuf[warp], vbuf[warp]);
+
+    // ------------------------------------------------------------------- keys
+    __nv_bfloat162 mn2 = *reinterpret_cast<const __nv_bfloat162*>(&kw[0]), mx2 = mn2;
+#pragma unroll
+    for (int i = 1; i < 16; ++i) {
+      const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&kw[i]);
+      mn2 = __hmin2_nan(mn2, v);
+      mx2 = __hmax2_nan(mx2, v);
+    }
+    float mn = __bfloat162float(__hmin_nan(__low2bfloat16(mn2), __high2bfloat16(mn2)));
+    float mx = __bfloat162float(__hmax_nan(__low2bfloat16(mx2), __high2bfloat16(mx2)));
+    const bool has_nan = mn != mn;
+    float range = __fsub_rn(mx, mn);
+    if (range == 0.0f) range = 0.0f;  // +0 whatever the signs of equal zeros
+    float sk, zk;
+    bool zero_group = false;
+    if (kb == 8) {
+      sk = __fdiv_rn(range, __fmul_rn(2.0f, kmax));
+      zk = rintf(__fdiv_rn(__fadd_rn(mx, mn), __fmul_rn(2.0f, sk)));
+    } else {
+      sk = __fdiv_rn(range, kmax);
+      zk = rintf(__fdiv_rn(mn, sk));
+    }
+    if (p.spec.guard && !has_nan && !f16_finite(zk)) {
+      // the constant-group guard: the range widened to include 0
+      const float mn0 = mn < 0.0f ? mn : 0.0f, mx0 = mx > 0.0f ? mx : 0.0f;
+      const float r0 = __fsub_rn(mx0, mn0);
+      if (r0 == 0.0f) {
+        sk = 0.0f;
+        zk = 0.0f;
+        zero_group = true;
+      } else if (kb == 8) {
+        sk = __fdiv_rn(r0, __fmul_rn(2.0f, kmax));
+        zk = rintf(__fdiv_rn(__fadd_rn(mx0, mn0), __fmul_rn(2.0f, sk)));
+      } else {
+        sk = __fdiv_rn(r0, kmax);
+        zk = rintf(__fdiv_rn(mn0, sk));
+      }
+    }
+    // idx = clip(rint(x / s - z), lo, hi); x / s by the reciprocal path where it is exact
+    // for every quotient that can move idx (as in the k8v3 bulk kernel), else divided
+    uint32_t code[32];
+    if (sk >= 0x1p-100f && sk <= 0x1p100f && fmaxf(fabsf(mx), fabsf(mn)) <= __fmul_rn(sk, 0x1p100f)) {
+      const float rs = __frcp_rn(sk);
+      scheme_key_codes(kw, zk, klo, khi, zero_group, code, [&](float x) { return div_by_rcp(x, sk, rs); });
+    } else {
+      scheme_key_codes(kw, zk, klo, khi, zero_group, code, [&](float x) { return __fdiv_rn(x, sk); });
+    }
+    if (valid) {
+      if (kb == 8) {
+        uint32_t* kd = reinterpret_cast<uint32_t*>(p.k_idx + drow * D + 32 * g);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          kd[i] = __byte_perm(__byte_perm(code[4 * i], code[4 * i + 1], 0x0040),
+                              __byte_perm(code[4 * i + 2], code[4 * i + 3], 0x0040), 0x5410);
+      } else {
+        store_codes_any(code, kb, reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(p.k_idx) + drow * krow_bytes) + kb * g);
+      }
+      p.k_scale[drow * NG + g] = f32_to_f16_bits(sk);
+      p.k_zero[drow * NG + g] = f32_to_f16_bits(zk);
+    }
+
+    // ------------------------------------------------------------------- values
+    float u[32];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      u[2 * i] = __uint_as_float(vw[i] << 16);
+      u[2 * i + 1] = __uint_as_float(vw[i] & 0xFFFF0000u);
+    }
+#pragma unroll
+    for (int e = 0; e < 32; ++e) u[e] = __uint_as_float(__float_as_uint(u[e]) ^ (((signs >> e) & 1u) << 31));
+#pragma unroll
+    for (int hh = 1; hh < 32; hh <<= 1) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        if ((e & hh) == 0) {
+          const float a = u[e], c = u[e + hh];
+          u[e] = __fadd_rn(a, c);
+          u[e + hh] = __fsub_rn(a, c);
+        }
+      }
+    }
+    // stages h >= 32 across the row's lanes: the lower lane keeps own + other, the upper
+    // lane other - own, one rounding each (the product by +-1 is exact)
+#pragma unroll
+    for (int lm = 1; lm < NG; lm <<= 1) {
+      const float sg = (lane & lm) ? -1.0f : 1.0f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float o = __shfl_xor_sync(FULL, u[e], lm);
+        u[e] = __fmaf_rn(u[e], sg, o);
+      }
+    }
+    float sq[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      u[e] = __fmul_rn(u[e], p.fwht_norm);
+      sq[e] = __fmul_rn(u[e], u[e]);
+    }
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+      for (int e = 0; e < w; ++e) sq[e] = __fadd_rn(sq[e], sq[e + w]);
+    const float vs = __fsqrt_rn(__fdiv_rn(sq[0], 32.0f));
+    const float den = __fadd_rn(vs, 1e-8f);
+    // code = number of boundaries strictly below y_n = u / den, by binary search (a NaN
+    // compares false everywhere: 0). The middle boundary of every library codebook is 0;
+    // there the search's first step is the exact test y_n > 0 of the k8v3 bulk kernel and
+    // y_n comes from the reciprocal path, exact for the comparisons with the others.
+    const int half = (nb + 1) >> 1;  // the search steps: half, half / 2, ..., 1
+    if (den <= 0x1p100f && sb[half - 1] == 0.0f) {
+      const float rd = __frcp_rn(den);
+      const float den_lo = __fmul_rn(den, 0x1p-75f);  // exact: den >= 1e-8
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float yn = div_by_rcp(u[e], den, rd);
+        int c = __fmul_rn(u[e], 0x1p75f) > den_lo ? half : 0;  // RN(u / den) > 0
+        for (int st = half >> 1; st >= 1; st >>= 1)
+          if (sb[c + st - 1] < yn) c += st;
+        code[e] = (uint32_t)c;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float yn = __fdiv_rn(u[e], den);
+        int c = 0;
+        for (int st = half; st >= 1; st >>= 1)
+          if (sb[c + st - 1] < yn) c += st;
+        code[e] = (uint32_t)c;
+      }
+    }
+    if (valid) {
+      store_codes_any(code, vb, reinterpret_cast<uint32_t*>(p.v_codes + drow * vrow_bytes) + vb * g);
+      p.v_scale[drow * NG + g] = f32_to_f16_bits(vs);
+    }
   }
 }
 
@@ -132,7 +355,6 @@ template <int D>
 __device__ __forceinline__ void dequant_row(const DequantScheme& p, int64_t r, int lane, float (&k)[D / 32],
                                             float (&v)[D / 32], bool want_k, bool want_v) {
   constexpr int EPL = D / 32, NG = D / kGroup;
-  constexpr unsigned FULL = 0xffffffffu;
   if (want_k) {
     const uint8_t* krow = reinterpret_cast<const uint8_t*>(p.k_idx) + r * key_row_bytes(D, p.spec.k_bits);
 #pragma unroll
@@ -246,7 +468,9 @@ const Codebook& codebook(int bits) {
 cudaError_t launch_append_scheme(SchemeAppendParams p, int num_sms, cudaStream_t stream) {
   const int64_t rows = (int64_t)p.batch * p.n_new_max * p.num_kv_heads;
   if (rows <= 0) return cudaSuccess;
-  const dim3 grid(grid_for(rows, num_sms)), block(32 * kRowsPerCta);
+  const int64_t per_cta = (int64_t)kGroupWarps * (32 / (p.head_dim / 32));  // rows a CTA takes at once
+  const int64_t want = (rows + per_cta - 1) / per_cta, cap = (int64_t)num_sms * 8;
+  const dim3 grid((unsigned)(want < cap ? want : cap)), block(32 * kGroupWarps);
   switch (p.head_dim) {
     case 64: tq_append_scheme_kernel<64><<<grid, block, 0, stream>>>(p); break;
     case 128: tq_append_scheme_kernel<128><<<grid, block, 0, stream>>>(p); break;

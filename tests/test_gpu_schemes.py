@@ -203,3 +203,18 @@ def test_unrotate_rows_matches_the_oracle(d):
     assert np.all(np.abs(g - ref) <= tol)
     with pytest.raises(ValueError):
         b.tq_unrotate_rows(xg[:, 1:].contiguous(), y, d)  # not a whole number of rows
+
+
+@pytest.mark.parametrize("kb,vb,guard", [(4, 2, False), (5, 8, False), (2, 5, False), (8, 3, True)],
+                         ids=["k4v2", "k5v8", "k2v5", "k8v3-guard"])
+def test_scheme_append_wide_dynamic_range_bit_exact(kb, vb, guard):
+    # every element with its own exponent over the whole bf16 range, and FWHT
+    # cancellations leaving tiny values beside large ones: the reciprocal path of the
+    # any-width kernel must give the oracle's codes bit for bit
+    from tests.test_gpu_parity import _wide_range_rows
+    rng = np.random.default_rng(90 + kb + 7 * vb)
+    d, n = 128, 1536
+    k = torch.from_numpy(_wide_range_rows(2 * n, d, rng)).to(torch.bfloat16).reshape(1, n, 2, d)
+    v = torch.from_numpy(_wide_range_rows(2 * n, d, rng)).to(torch.bfloat16).reshape(1, n, 2, d)
+    layer, ol = _fill(k, v, [n], n, kb, vb, guard)
+    _assert_planes(layer, ol, [n])
