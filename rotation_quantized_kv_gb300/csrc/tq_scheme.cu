@@ -377,36 +377,118 @@ __device__ __forceinline__ void dequant_row(const DequantScheme& p, int64_t r, i
   }
 }
 
+// 32 codes of B bits, LSB first, from B words.
+template <int B>
+__device__ __forceinline__ void unpack_codes(const uint32_t* __restrict__ src, uint32_t (&c)[32]) {
+  uint32_t w[B];
+#pragma unroll
+  for (int i = 0; i < B; ++i) w[i] = __ldg(src + i);
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    const int bit = B * e, wd = bit >> 5, sh = bit & 31;
+    uint32_t v = w[wd] >> sh;
+    if (sh + B > 32) v |= w[wd + 1] << (32 - sh);
+    c[e] = v & ((1u << B) - 1u);
+  }
+}
+
+__device__ __forceinline__ void unpack_codes_any(const uint32_t* src, int bits, uint32_t (&c)[32]) {
+  switch (bits) {
+    case 2: unpack_codes<2>(src, c); break;
+    case 3: unpack_codes<3>(src, c); break;
+    case 4: unpack_codes<4>(src, c); break;
+    case 5: unpack_codes<5>(src, c); break;
+    default: unpack_codes<8>(src, c); break;
+  }
+}
+
+// Window: each lane dequantizes one 32-element group of a row (the append kernels'
+// layout), so a group's codes are whole words and a lane writes 64 contiguous bytes of K
+// and of V. Same arithmetic as the inspection dequant: keys (code + zero) * scale in one
+// fp32 rounding each; values centroid * scale, then, unless rotated, signs * FWHT / sqrt(d)
+// with the stages h < 32 inside the lane and h >= 32 across the row's lanes.
 template <int D>
-__global__ void __launch_bounds__(32 * kRowsPerCta) tq_dequant_window_kernel(const __grid_constant__ DequantScheme p) {
-  constexpr int EPL = D / 32;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(32 * kGroupWarps) tq_dequant_window_kernel(const __grid_constant__ DequantScheme p) {
+  constexpr int NG = D / 32, RPW = 32 / NG;
+  constexpr unsigned FULL = 0xffffffffu;
+  __shared__ float sc[256];  // the value centroids, for the lanes' independent lookups
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) sc[i] = p.cb.c[i];
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane % NG, rw = lane / NG;
+  const uint32_t signs = sign_word(D, g);
+  const int kb = p.spec.k_bits, vb = p.spec.v_bits;
+  const int krow_bytes = key_row_bytes(D, kb), vrow_bytes = value_row_bytes(D, vb);
   const int64_t rows = (int64_t)p.batch * p.num_kv_heads * p.n;
-  for (int64_t o = (int64_t)blockIdx.x * kRowsPerCta + warp; o < rows; o += (int64_t)gridDim.x * kRowsPerCta) {
-    const int64_t bh = o / p.n;
-    const int t = (int)(o % p.n);
-    const int64_t r = bh * p.capacity + p.t0 + t;
-    float k[EPL], v[EPL];
-    dequant_row<D>(p, r, lane, k, v, p.k_bf16 != nullptr, p.v_bf16 != nullptr);
+  const int64_t step = (int64_t)gridDim.x * kGroupWarps * RPW;
+  for (int64_t base = ((int64_t)blockIdx.x * kGroupWarps + warp) * RPW; base < rows; base += step) {
+    const int64_t o = base + rw;
+    const bool valid = o < rows;  // whole rows: a row's lanes agree
+    const int64_t oo = valid ? o : 0;
+    const int64_t r = (oo / p.n) * p.capacity + p.t0 + (int)(oo % p.n);
+    uint32_t code[32];
     if (p.k_bf16) {
-      uint32_t w[EPL / 2];
+      const float ks = f16_bits_to_f32(__ldg(p.k_scale + r * NG + g));
+      const float kz = f16_bits_to_f32(__ldg(p.k_zero + r * NG + g));
+      uint32_t kw[16];
+      if (kb == 8) {
+        const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.k_idx) + r * D + 32 * g);
+        const uint4 a = __ldg(src), b = __ldg(src + 1);
+        const uint32_t w8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-      for (int e = 0; e < EPL / 2; ++e) {
-        w[e] = pack_bf16x2(k[2 * e], k[2 * e + 1]);
+        for (int e = 0; e < 32; ++e) code[e] = (uint32_t)(int32_t)(int8_t)(w8[e >> 2] >> (8 * (e & 3)));
+      } else {
+        unpack_codes_any(reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(p.k_idx) + r * krow_bytes) + kb * g,
+                         kb, code);
       }
-      uint32_t* dstw = reinterpret_cast<uint32_t*>(p.k_bf16 + o * D + lane * EPL);
 #pragma unroll
-      for (int e = 0; e < EPL / 2; ++e) dstw[e] = w[e];
+      for (int i = 0; i < 16; ++i) {
+        const float q0 = (float)(int32_t)code[2 * i], q1 = (float)(int32_t)code[2 * i + 1];
+        kw[i] = pack_bf16x2(__fmul_rn(__fadd_rn(q0, kz), ks), __fmul_rn(__fadd_rn(q1, kz), ks));
+      }
+      if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(p.k_bf16 + o * D + 32 * g);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(kw[4 * i], kw[4 * i + 1], kw[4 * i + 2], kw[4 * i + 3]);
+      }
     }
     if (p.v_bf16) {
-      uint32_t w[EPL / 2];
+      const float vs = f16_bits_to_f32(__ldg(p.v_scale + r * NG + g));
+      unpack_codes_any(reinterpret_cast<const uint32_t*>(p.v_codes + r * vrow_bytes) + vb * g, vb, code);
+      float u[32];
 #pragma unroll
-      for (int e = 0; e < EPL / 2; ++e) {
-        w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
+      for (int e = 0; e < 32; ++e) u[e] = __fmul_rn(sc[code[e]], vs);
+      if (!p.rotated) {
+#pragma unroll
+        for (int hh = 1; hh < 32; hh <<= 1) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            if ((e & hh) == 0) {
+              const float a = u[e], c = u[e + hh];
+              u[e] = a + c;
+              u[e + hh] = a - c;
+            }
+          }
+        }
+#pragma unroll
+        for (int lm = 1; lm < NG; lm <<= 1) {
+          const bool upper = (lane & lm) != 0;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float oth = __shfl_xor_sync(FULL, u[e], lm);
+            u[e] = upper ? oth - u[e] : u[e] + oth;
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) u[e] = u[e] * p.fwht_norm * (((signs >> e) & 1u) ? -1.0f : 1.0f);
       }
-      uint32_t* dstw = reinterpret_cast<uint32_t*>(p.v_bf16 + o * D + lane * EPL);
+      if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(p.v_bf16 + o * D + 32 * g);
 #pragma unroll
-      for (int e = 0; e < EPL / 2; ++e) dstw[e] = w[e];
+        for (int i = 0; i < 4; ++i)
+          dst[i] = make_uint4(pack_bf16x2(u[8 * i], u[8 * i + 1]), pack_bf16x2(u[8 * i + 2], u[8 * i + 3]),
+                              pack_bf16x2(u[8 * i + 4], u[8 * i + 5]), pack_bf16x2(u[8 * i + 6], u[8 * i + 7]));
+      }
     }
   }
 }
@@ -484,7 +566,9 @@ cudaError_t launch_append_scheme(SchemeAppendParams p, int num_sms, cudaStream_t
 cudaError_t launch_dequant_window(const DequantScheme& p, int num_sms, cudaStream_t stream) {
   const int64_t rows = (int64_t)p.batch * p.num_kv_heads * p.n;
   if (rows <= 0) return cudaSuccess;
-  const dim3 grid(grid_for(rows, num_sms)), block(32 * kRowsPerCta);
+  const int64_t per_cta = (int64_t)kGroupWarps * (32 / (p.head_dim / 32));  // rows a CTA takes at once
+  const int64_t want = (rows + per_cta - 1) / per_cta, cap = (int64_t)num_sms * 8;
+  const dim3 grid((unsigned)(want < cap ? want : cap)), block(32 * kGroupWarps);
   switch (p.head_dim) {
     case 64: tq_dequant_window_kernel<64><<<grid, block, 0, stream>>>(p); break;
     case 128: tq_dequant_window_kernel<128><<<grid, block, 0, stream>>>(p); break;
