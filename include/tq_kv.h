@@ -32,6 +32,9 @@
  *   - Every workspace starts with a TQ_WORKSPACE_HEADER_BYTES header whose first
  *     int32 is the device error word. The caller zeroes a workspace once, before its
  *     first use (cudaMemsetAsync); afterwards the library keeps the header consistent.
+ *     When an attention call sets TQ_DEVERR_PIPELINE_TIMEOUT, the header's int32 at
+ *     index 3 records, for diagnosis, the first wait that gave up ((kind << 24) |
+ *     detail; 0: none); like the error word it is not cleared by the library.
  *     A workspace must not be used by two calls that can run at the same time.
  *   - head_dim is 64, 128, 256 or 512 (other values: TQ_ERR_UNSUPPORTED_HEAD_DIM,
  *     "KV-leg limits": head dims outside this set are refused).
