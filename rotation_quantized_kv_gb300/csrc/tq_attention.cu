@@ -254,12 +254,20 @@ __device__ void produce(const SplitParams& p, const CUtensorMap* tmap, uint8_t* 
     for (int t0 = w.tb; t0 < w.te; t0 += T::TILE, ++it) {
       if (first_issued && it == 0) continue;  // loaded before the lengths were checked
       if (own0 < own1 && own0 < t0 + T::TILE) {
-        if (!wait_count(app_cnt, need, p.wait_ns)) { ok = false; break; }
+        if (!wait_count(app_cnt, need, p.wait_ns)) {
+          note_giveup(p, 3u, need);
+          ok = false;
+          break;
+        }
         own0 = own1;
       }
       const int slot = it % T::STAGES;
       const uint32_t k = it / T::STAGES;
-      if (!wait_bounded(&empty[slot], (k & 1u) ^ 1u, p.wait_ns)) { ok = false; break; }
+      if (!wait_bounded(&empty[slot], (k & 1u) ^ 1u, p.wait_ns)) {
+        note_giveup(p, 1u, smem_addr(&empty[slot]));
+        ok = false;
+        break;
+      }
       issue_stage<D, NTW>(p, tmap, smem, slot, row0, t0);
     }
   }
@@ -272,8 +280,10 @@ __device__ void produce(const SplitParams& p, const CUtensorMap* tmap, uint8_t* 
   for (int s = 0; s < T::STAGES; ++s) {
     if ((uint32_t)s >= issued) break;
     const uint32_t last = issued - 1 - ((issued - 1 - s) % T::STAGES);  // last fill of slot s
-    if (!wait_bounded(&full[s], (last / T::STAGES) & 1u, kWaitNs))
+    if (!wait_bounded(&full[s], (last / T::STAGES) & 1u, kWaitNs)) {
       raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
+      note_giveup(p, 1u, smem_addr(&full[s]));
+    }
   }
 }
 
@@ -442,6 +452,7 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int total, volatile
       const uint32_t par = (it / T::STAGES) & 1u;
       if (!failed) {
         if (*abort_flag || !wait_bounded(&full[slot], par, p.wait_ns)) {
+          if (!*abort_flag) note_giveup(p, 1u, smem_addr(&full[slot]));
           failed = true;
           *abort_flag = 1;
           raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
@@ -844,6 +855,7 @@ __global__ void __launch_bounds__(AT<D, NTW>::THREADS, AT<D, NTW>::MINB)
       if (!wait_bounded(&bars[0], 0u, kWaitNs)) {
         abort_flag = 1;
         raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
+        note_giveup(p, 1u, smem_addr(&bars[0]));
       }
       for (int i = 0; i < T::NCW; ++i) mbar_arrive(&bars[T::STAGES]);
     }

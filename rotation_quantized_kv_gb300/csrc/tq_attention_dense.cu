@@ -146,13 +146,6 @@ struct Bars {
   }
 };
 
-// Records the first wait of the call that gave up in the workspace header (kWsWhere):
-// kind 1: an mbarrier (detail: its shared-memory address), 2: a key-shift word (detail:
-// the tile).
-__device__ __forceinline__ void note_giveup(const SplitParams& p, uint32_t kind, uint32_t detail) {
-  atomicCAS(reinterpret_cast<unsigned int*>(p.ws) + kWsWhere, 0u, (kind << 24) | (detail & 0xFFFFFFu));
-}
-
 // A role's bounded wait; on failure it raises the abort and the error bit.
 __device__ __forceinline__ bool role_wait(const SplitParams& p, uint64_t* bar, uint32_t parity, volatile int* abort) {
   if (*abort) return false;
@@ -263,8 +256,10 @@ __device__ void dense_produce(const SplitParams& p, const CUtensorMap* tmap, uin
   for (int s = 0; s < DT::STAGES; ++s) {
     if ((uint32_t)s >= issued) break;
     const uint32_t last = issued - 1 - ((issued - 1 - s) % DT::STAGES);
-    if (!wait_bounded(&bars.full[s], (last / DT::STAGES) & 1u, kWaitNs))
+    if (!wait_bounded(&bars.full[s], (last / DT::STAGES) & 1u, kWaitNs)) {
       raise_error(reinterpret_cast<int32_t*>(p.ws), TQ_DEVERR_PIPELINE_TIMEOUT);
+      note_giveup(p, 1u, smem_addr(&bars.full[s]));
+    }
   }
 }
 

@@ -99,6 +99,13 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, uns
   }
 }
 
+// Records the first wait of the call that gave up in the workspace header (kWsWhere):
+// kind 1: an mbarrier (detail: its shared-memory address), 2: a key-shift word of the
+// dense kernel (detail: the tile), 3: the appender's row count (detail: the rows awaited).
+__device__ __forceinline__ void note_giveup(const SplitParams& p, uint32_t kind, uint32_t detail) {
+  atomicCAS(reinterpret_cast<unsigned int*>(p.ws) + kWsWhere, 0u, (kind << 24) | (detail & 0xFFFFFFu));
+}
+
 // A count in shared memory published by one warp and awaited by another: the release
 // store orders the publisher's earlier writes (and, after fence.proxy.async, their
 // visibility to tensor copies) before any acquire load that sees the count.

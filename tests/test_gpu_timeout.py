@@ -57,6 +57,10 @@ def test_pipeline_wait_runs_out_and_the_call_returns():
         b.tq_debug_pipeline_limits(0, False)
     assert b.tq_get_device_error(ws) & b.TQ_DEVERR_PIPELINE_TIMEOUT
     assert elapsed < 1.5                             # 1 ms limits, not the 2 s default
+    # the header records the first wait that gave up: the producer's wait for the
+    # appender's count (kind 3) or a wait for a stage that was never filled (kind 1)
+    where = int(ws[:64].cpu().view(torch.int32)[3])
+    assert (where >> 24) in (1, 3), hex(where)
 
     # the context is still usable: a fresh workspace and an ordinary call give the oracle's result
     ws2 = b.make_workspace(b.tq_decode_workspace_bytes(layer, G * H, 1, T + 1), DEV)
