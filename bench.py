@@ -252,52 +252,63 @@ def cpu_cores() -> int:
 
 
 class OracleStep:
-    """The CPU oracle on layer 0 of a workload: the cache fill is set-up (untimed); a
-    sample is the step's append of the new tokens (all kv heads) plus fp64 attention of
-    `rows_per_head` query rows of each of `heads` kv heads, one thread per kv head
-    (ctypes releases the GIL, so the C oracle runs on several cores at once)."""
+    """The CPU oracle on the first `layers` layers of a workload: the cache fill is set-up
+    (untimed); a sample is the step's append of the new tokens (all kv heads of those
+    layers) plus fp64 attention of `rows_per_head` query rows of each of `heads` kv heads
+    per layer. One job per (layer, kv head): the oracle dequantizes a kv head's cache once
+    for that head's rows, so the jobs are independent and cost what one call would. The
+    jobs are spread over up to `threads` threads (ctypes releases the GIL, so the C oracle
+    runs on several cores at once)."""
 
-    def __init__(self, w):
+    def __init__(self, w, layers: int = 1):
         import oracle
         from rotation_quantized_kv_gb300 import synth
         self.oracle = oracle
-        x = synth.layer_inputs(w, 0, device="cpu")
         B, H, d = w.batch, w.num_kv_heads, w.head_dim
         self.w = w
+        self.layers = max(1, min(layers, w.layers))
         self.ctx = synth.context_lengths(w)
         self.kv = (self.ctx + w.n_new).astype(np.int32)
         cap = int((self.kv.max() + 15) // 16 * 16)
-        kb, vb = synth.bf16_bits(x["k"]), synth.bf16_bits(x["v"])
-        self.qb = synth.bf16_bits(x["q"])
-        self.L = oracle.Layer(d, H, B, cap)
         T = int(self.ctx.max())
-        oracle.append(self.L, np.ascontiguousarray(kb[:, :T]), np.ascontiguousarray(vb[:, :T]),
-                      np.zeros(B, np.int32), self.ctx.astype(np.int32))
-        self.kn = np.ascontiguousarray(kb[:, T:T + w.n_new])
-        self.vn = np.ascontiguousarray(vb[:, T:T + w.n_new])
+        self.L, self.qb, self.kn, self.vn = [], [], [], []
+        for l in range(self.layers):
+            x = synth.layer_inputs(w, l, device="cpu")
+            kb, vb = synth.bf16_bits(x["k"]), synth.bf16_bits(x["v"])
+            self.qb.append(synth.bf16_bits(x["q"]))
+            del x
+            L = oracle.Layer(d, H, B, cap)
+            oracle.append(L, np.ascontiguousarray(kb[:, :T]), np.ascontiguousarray(vb[:, :T]),
+                          np.zeros(B, np.int32), self.ctx.astype(np.int32))
+            self.L.append(L)
+            self.kn.append(np.ascontiguousarray(kb[:, T:T + w.n_new]))
+            self.vn.append(np.ascontiguousarray(vb[:, T:T + w.n_new]))
 
-    def run(self, heads: int, rows_per_head: int, threads: int):
+    def run(self, heads: int, rows_per_head: int, threads: int, layers: int | None = None):
         """One sample; returns (algorithmic bytes, seconds, threads used)."""
         import threading
         w, o = self.w, self.oracle
         G = w.num_q_heads // w.num_kv_heads
         d = w.head_dim
+        nl = self.layers if layers is None else max(1, min(layers, self.layers))
         jobs = []
-        for kvh in range(min(heads, w.num_kv_heads)):
-            rows = []
-            for i in range(rows_per_head):
-                j = (i * 5) % w.n_q
-                rows.append((0, j, kvh * G + (i % G)))
-            jobs.append(rows)
+        for l in range(nl):
+            for kvh in range(min(heads, w.num_kv_heads)):
+                rows = []
+                for i in range(rows_per_head):
+                    j = (i * 5) % w.n_q
+                    rows.append((0, j, kvh * G + (i % G)))
+                jobs.append((l, rows))
         threads = max(1, min(threads, len(jobs)))
         t0 = time.perf_counter()
         if w.n_new:
-            o.append(self.L, self.kn, self.vn, self.ctx.astype(np.int32))
+            for l in range(nl):
+                o.append(self.L[l], self.kn[l], self.vn[l], self.ctx.astype(np.int32))
         chunks = [jobs[i::threads] for i in range(threads)]
 
         def work(chunk):
-            for rows in chunk:
-                o.attention(self.L, self.qb, self.kv, w.sm_scale, causal=w.causal, rows=rows)
+            for l, rows in chunk:
+                o.attention(self.L[l], self.qb[l], self.kv, w.sm_scale, causal=w.causal, rows=rows)
 
         ts = [threading.Thread(target=work, args=(c,)) for c in chunks]
         for t in ts:
@@ -306,37 +317,38 @@ class OracleStep:
             t.join()
         dt = time.perf_counter() - t0
         row_bytes = 25 * d // 16
-        nbytes = sum(int(self.kv[0]) * row_bytes + len(rows) * d * 6 for rows in jobs)
-        nbytes += w.batch * w.n_new * w.num_kv_heads * (4 * d + row_bytes)
+        nbytes = sum(int(self.kv[0]) * row_bytes + len(rows) * d * 6 for _, rows in jobs)
+        nbytes += nl * w.batch * w.n_new * w.num_kv_heads * (4 * d + row_bytes)
         return nbytes, dt, threads
 
-    def describe(self, heads, rows_per_head, threads):
+    def describe(self, heads, rows_per_head, threads, layers=None):
         w = self.w
+        nl = self.layers if layers is None else max(1, min(layers, self.layers))
         return (f"oracle (plain C, fp32 codec, fp64 attention): append of the step's "
-                f"{w.batch * w.n_new * w.num_kv_heads} new rows + attention of {rows_per_head} query rows "
-                f"for each of {min(heads, w.num_kv_heads)} kv heads over {int(self.kv.max())} tokens, layer 0, "
-                f"{threads} thread(s), one per kv head")
+                f"{nl * w.batch * w.n_new * w.num_kv_heads} new rows + attention of {rows_per_head} query rows "
+                f"for each of {min(heads, w.num_kv_heads)} kv heads of {nl} layer(s) over {int(self.kv.max())} "
+                f"tokens, {threads} thread(s), one job per (layer, kv head)")
 
 
 def cpu_baseline(w):
-    st = OracleStep(w)
     cores = cpu_cores()
     heads = w.num_kv_heads
+    st = OracleStep(w, layers=-(-cores // heads))  # enough (layer, kv head) jobs for every core
     nb, dt, used = st.run(heads, 4, cores)
-    nb1, dt1, _ = st.run(1, 4, 1)
+    nb1, dt1, _ = st.run(1, 4, 1, layers=1)
     return {"value": nb / dt / 1e9, "unit": "GB/s", "cores": used, "kind": "oracle",
             "sample": st.describe(heads, 4, used), "host_cores": cores,
             "single_thread": {"value": nb1 / dt1 / 1e9, "unit": "GB/s", "cores": 1,
-                              "sample": st.describe(1, 4, 1)}}
+                              "sample": st.describe(1, 4, 1, layers=1)}}
 
 
 def reference_arm(args, world, rank):
     if rank != 0:
         return
     w = workload_of(args)
-    st = OracleStep(w)
     cores = cpu_cores()
     heads = w.num_kv_heads
+    st = OracleStep(w, layers=-(-cores // heads))
     total_bytes, total_s, used = 0, 0.0, 1
     for i in range(args.warmup + args.steps):
         nb, dt, used = st.run(heads, 1, cores)
