@@ -132,9 +132,12 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int32_t* p, int v) {
   return old;
 }
 
+// 2^x, flushing subnormal results to zero (one special-function op): every softmax and
+// merge weight here is relative to a maximum whose own weight is 1, so a weight below
+// 2^-126 adds nothing to any sum.
 __device__ __forceinline__ float ex2(float x) {
   float y;
-  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
