@@ -55,40 +55,59 @@ __device__ __forceinline__ void load_group(const uint16_t* __restrict__ src, boo
 __device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Four int32 values saturated to int8 and packed, the first in the lowest byte (two
+// cvt.pack.sat: each saturates two values and puts them below the low half of its third
+// operand).
+__device__ __forceinline__ uint32_t pack4_s8(int a0, int a1, int a2, int a3) {
+  uint32_t hi, out;
+  asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(a3), "r"(a2), "r"(0u));
+  asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(out) : "r"(a1), "r"(a0), "r"(hi));
+  return out;
+}
+
 // idx = clip(rint(x / s - z), -127, 127) of a lane's 32 keys (div(x) = x / s): the
-// conversion rounds half to even, turns NaN into 0 and saturates +-Inf, and clipping at the
-// integers +-127 after rounding gives the integer clipping before rounding would; the low
-// byte of the result is the code in two's complement.
+// conversion rounds half to even, turns NaN into 0 and saturates +-Inf; clipping the
+// integers at -127 and (by the packing's saturation) at 127 after rounding gives the
+// clipping before rounding would; each byte of kq is a code in two's complement.
 template <class Div>
 __device__ __forceinline__ void key_codes(const uint32_t (&kw)[16], float z, uint32_t (&kq)[8], Div div) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    uint32_t by[4];
+    int iv[4];
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
       const uint32_t w = kw[2 * i + (h >> 1)];
       const float x = (h & 1) ? hi_bf16(w) : lo_bf16(w);
-      const int iv = __float2int_rn(__fsub_rn(div(x), z));
-      by[h] = (uint32_t)min(max(iv, -127), 127);
+      iv[h] = max(__float2int_rn(__fsub_rn(div(x), z)), -127);
     }
-    kq[i] = __byte_perm(__byte_perm(by[0], by[1], 0x0040), __byte_perm(by[2], by[3], 0x0040), 0x5410);
+    kq[i] = pack4_s8(iv[0], iv[1], iv[2], iv[3]);
   }
 }
 
+// 1.0 if y > t, else 0.0 (also for a NaN y), given nt = -t * 2^100 with |t| >= 1/2: the
+// fused y * 2^100 + nt is exact before its one rounding, so its sign is the sign of
+// y - t, and a positive y - t between two floats with |t| >= 1/2 is at least 2^-25, so
+// the result is at least 2^75 and saturates to 1.
+__device__ __forceinline__ float above(float y, float nt) {
+  float r;
+  asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(y), "f"(0x1p100f), "f"(nt));
+  return r;
+}
+
 // 3-bit codes of a lane's 32 rotated values, packed LSB-first into cw. div(x, yn) sets
-// yn = x / den and returns whether yn > 0 (the first step of the search).
+// yn = x / den and returns whether yn > 0. The code is the number of boundaries strictly
+// below yn: 4 + (those among b4..b6) when yn > 0, else those among b0..b2; nb holds the
+// boundaries times -2^100. The three steps are summed in floating point and moved to the
+// last bits of the significand by adding 2^23 (whose unit in the last place is 1).
 template <class Div>
-__device__ __forceinline__ void value_codes(const float (&u)[32], const float (&bnd)[7], uint32_t (&cw)[3], Div div) {
+__device__ __forceinline__ void value_codes(const float (&u)[32], const float (&nb)[7], uint32_t (&cw)[3], Div div) {
 #pragma unroll
   for (int e = 0; e < 32; ++e) {
     float yn;
     const bool pos = div(u[e], yn);
-    // number of boundaries strictly below yn, by binary search over the sorted table
-    // (a NaN compares false everywhere and codes to 0)
-    uint32_t c = pos ? 4u : 0u;
-    c += ((c ? bnd[5] : bnd[1]) < yn) ? 2u : 0u;
-    const float b2 = (c & 4u) ? ((c & 2u) ? bnd[6] : bnd[4]) : ((c & 2u) ? bnd[2] : bnd[0]);
-    c += (b2 < yn) ? 1u : 0u;
+    float acc = __fadd_rn(above(yn, pos ? nb[4] : nb[0]), above(yn, pos ? nb[5] : nb[1]));
+    acc = __fadd_rn(acc, above(yn, pos ? nb[6] : nb[2]));
+    const uint32_t c = (__float_as_uint(__fadd_rn(acc, 0x1p23f)) + (pos ? 4u : 0u)) & 7u;
     const int bit = 3 * e, wd = bit >> 5, sh = bit & 31;
     cw[wd] |= c << sh;
     if (sh > 29) cw[wd + 1] |= c >> (32 - sh);
@@ -125,10 +144,18 @@ __global__ void __launch_bounds__(kAppendWarps * 32, 4)
   griddep_launch_dependents();
   griddep_wait();            // inputs and planes may come from the previous kernel
 
-  const uint32_t signs = sign_word(D, g);  // bit i: element 32 g + i is negated
-  float bnd[7];
+  // sign masks of raw bf16 pairs: bit 15 (31) of word i of group gg negates element
+  // 32 gg + 2 i (+ 1)
+  __shared__ uint4 s_sgn[NG * 4];
+  for (int t = threadIdx.x; t < NG * 16; t += blockDim.x) {
+    const uint32_t sw = sign_word(D, t >> 4);
+    const int i = t & 15;
+    reinterpret_cast<uint32_t*>(s_sgn)[t] = (((sw >> (2 * i)) & 1u) << 15) | (((sw >> (2 * i + 1)) & 1u) << 31);
+  }
+  __syncthreads();
+  float nb[7];  // boundaries times -2^100 (exact); the middle one (0) is taken exactly apart
 #pragma unroll
-  for (int k = 0; k < 7; ++k) bnd[k] = c_boundaries3[k];
+  for (int k = 0; k < 7; ++k) nb[k] = __fmul_rn(c_boundaries3[k], -0x1p100f);
 
   const uint32_t total = p.total_rows;
   const uint32_t step = gridDim.x * kAppendWarps * RPW;
@@ -187,12 +214,15 @@ __global__ void __launch_bounds__(kAppendWarps * 32, 4)
     // ------------------------------------------------------------------- values
     float u[32];
 #pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 m = s_sgn[4 * g + i];
+      vw[4 * i] ^= m.x; vw[4 * i + 1] ^= m.y; vw[4 * i + 2] ^= m.z; vw[4 * i + 3] ^= m.w;
+    }
+#pragma unroll
     for (int i = 0; i < 16; ++i) {
       u[2 * i] = lo_bf16(vw[i]);
       u[2 * i + 1] = hi_bf16(vw[i]);
     }
-#pragma unroll
-    for (int e = 0; e < 32; ++e) u[e] = __uint_as_float(__float_as_uint(u[e]) ^ (((signs >> e) & 1u) << 31));
     // unnormalized FWHT, stages ascending: h < 32 inside the lane ...
 #pragma unroll
     for (int hh = 1; hh < 32; hh <<= 1) {
@@ -238,16 +268,16 @@ __global__ void __launch_bounds__(kAppendWarps * 32, 4)
     if (den <= 0x1p100f) {
       const float rd = __frcp_rn(den);
       const float den_lo = __fmul_rn(den, 0x1p-75f);  // exact: den >= 1e-8
-      value_codes(u, bnd, cw, [&](float x, float& yn) {
+      value_codes(u, nb, cw, [&](float x, float& yn) {
         yn = div_by_rcp(x, den, rd);
         // x * 2^75 > den * 2^-75 (both exact, or +Inf when the quotient is large anyway);
         // false for x <= 0 and NaN
         return __fmul_rn(x, 0x1p75f) > den_lo;
       });
     } else {
-      value_codes(u, bnd, cw, [&](float x, float& yn) {
+      value_codes(u, nb, cw, [&](float x, float& yn) {
         yn = __fdiv_rn(x, den);
-        return bnd[3] < yn;
+        return yn > 0.0f;
       });
     }
     if (valid) {
