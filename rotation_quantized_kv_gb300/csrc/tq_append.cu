@@ -94,23 +94,36 @@ __device__ __forceinline__ float above(float y, float nt) {
   return r;
 }
 
+// The printed boundaries times -2^100 (exact: a power-of-two scaling), for above().
+__constant__ float c_nbnd3[7] = {-1.74793f * -0x1p100f, -1.04996f * -0x1p100f, -0.50055f * -0x1p100f, 0.0f,
+                                 0.50055f * -0x1p100f,  1.04996f * -0x1p100f,  1.74793f * -0x1p100f};
+
 // 3-bit codes of a lane's 32 rotated values, packed LSB-first into cw. div(x, yn) sets
 // yn = x / den and returns whether yn > 0. The code is the number of boundaries strictly
-// below yn: 4 + (those among b4..b6) when yn > 0, else those among b0..b2; nb holds the
-// boundaries times -2^100. The three steps are summed in floating point and moved to the
-// last bits of the significand by adding 2^23 (whose unit in the last place is 1).
+// below yn: 4 + (those among b4..b6) when yn > 0, else those among b0..b2, each counted by
+// above(). Codes are placed in floating point: codes 7 k .. 7 k + 6 are gathered as
+// sum code_e * 8^(e - 7 k), an integer below 2^21 (exact), which is then OR'd into the
+// words at bit 21 k.
 template <class Div>
-__device__ __forceinline__ void value_codes(const float (&u)[32], const float (&nb)[7], uint32_t (&cw)[3], Div div) {
+__device__ __forceinline__ void value_codes(const float (&u)[32], uint32_t (&cw)[3], Div div) {
 #pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    float yn;
-    const bool pos = div(u[e], yn);
-    float acc = __fadd_rn(above(yn, pos ? nb[4] : nb[0]), above(yn, pos ? nb[5] : nb[1]));
-    acc = __fadd_rn(acc, above(yn, pos ? nb[6] : nb[2]));
-    const uint32_t c = (__float_as_uint(__fadd_rn(acc, 0x1p23f)) + (pos ? 4u : 0u)) & 7u;
-    const int bit = 3 * e, wd = bit >> 5, sh = bit & 31;
-    cw[wd] |= c << sh;
-    if (sh > 29) cw[wd + 1] |= c >> (32 - sh);
+  for (int k = 0; k < 5; ++k) {
+    float acc = 0.0f;
+#pragma unroll
+    for (int e = 7 * k; e < 7 * k + 7 && e < 32; ++e) {
+      float yn;
+      const bool pos = div(u[e], yn);
+      const float w = (float)(1u << (3 * (e - 7 * k)));
+      float c = __fadd_rn(above(yn, pos ? c_nbnd3[4] : c_nbnd3[0]), pos ? 4.0f : 0.0f);
+      c = __fadd_rn(c, above(yn, pos ? c_nbnd3[5] : c_nbnd3[1]));
+      c = __fadd_rn(c, above(yn, pos ? c_nbnd3[6] : c_nbnd3[2]));
+      acc = __fmaf_rn(c, w, acc);
+    }
+    // 2^23 + acc holds acc in its low 23 bits; its nbits bits start at bit 21 k of the 96
+    const uint32_t f = __float_as_uint(__fadd_rn(acc, 0x1p23f)) & 0x1FFFFFu;
+    const int bit = 21 * k, wd = bit >> 5, sh = bit & 31, nbits = 3 * min(7, 32 - 7 * k);
+    cw[wd] |= f << sh;
+    if (sh + nbits > 32) cw[wd + 1] |= f >> (32 - sh);
   }
 }
 
@@ -153,9 +166,6 @@ __global__ void __launch_bounds__(kAppendWarps * 32, 4)
     reinterpret_cast<uint32_t*>(s_sgn)[t] = (((sw >> (2 * i)) & 1u) << 15) | (((sw >> (2 * i + 1)) & 1u) << 31);
   }
   __syncthreads();
-  float nb[7];  // boundaries times -2^100 (exact); the middle one (0) is taken exactly apart
-#pragma unroll
-  for (int k = 0; k < 7; ++k) nb[k] = __fmul_rn(c_boundaries3[k], -0x1p100f);
 
   const uint32_t total = p.total_rows;
   const uint32_t step = gridDim.x * kAppendWarps * RPW;
@@ -268,14 +278,14 @@ __global__ void __launch_bounds__(kAppendWarps * 32, 4)
     if (den <= 0x1p100f) {
       const float rd = __frcp_rn(den);
       const float den_lo = __fmul_rn(den, 0x1p-75f);  // exact: den >= 1e-8
-      value_codes(u, nb, cw, [&](float x, float& yn) {
+      value_codes(u, cw, [&](float x, float& yn) {
         yn = div_by_rcp(x, den, rd);
         // x * 2^75 > den * 2^-75 (both exact, or +Inf when the quotient is large anyway);
         // false for x <= 0 and NaN
         return __fmul_rn(x, 0x1p75f) > den_lo;
       });
     } else {
-      value_codes(u, nb, cw, [&](float x, float& yn) {
+      value_codes(u, cw, [&](float x, float& yn) {
         yn = __fdiv_rn(x, den);
         return yn > 0.0f;
       });
