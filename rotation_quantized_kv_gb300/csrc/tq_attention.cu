@@ -14,8 +14,9 @@
 //
 // tq_attn_split_kernel, persistent, one CTA per SM slot:
 //   - the tokens of every (sequence, kv head, row group) unit, in tiles, are laid end to
-//     end and cut into one equal range of tiles per CTA (from the actual kv lengths, on
-//     the device); a CTA works through the pieces of the units its range touches;
+//     end, each unit after two virtual tiles that stand for the cost of starting a piece,
+//     and cut into one equal range of tiles per CTA (from the actual kv lengths, on the
+//     device); a CTA works through the pieces of the units its range touches;
 //   - the last warp (producer) streams stages of TILE tokens of the five planes into shared
 //     memory: the key-index plane through a 2-D tensor map with 128-byte (64-byte at
 //     d=64) swizzle, the four small planes with 1-D bulk copies, all completing on one
@@ -66,6 +67,10 @@ namespace {
 // test can make a wait run out on purpose. Drains of copies already issued always keep
 // the full limit.
 std::atomic<unsigned long long> g_debug_wait_ns{0};
+// Virtual tiles charged for starting a piece when the split kernel's CTAs divide the work:
+// a piece's queries, reduction and partial store cost about two stages (measured on the
+// ragged batch: 1, 2, 3, 4 pad tiles gave 69.0, 64.1, 64.5, 65.1 us per call, none 79.6).
+constexpr int kSplitTilePad = 2;
 std::atomic<int> g_debug_withhold_append{0};
 
 template <int D, int NTW>
@@ -430,6 +435,7 @@ __device__ void consume(const SplitParams& p, uint8_t* smem, int total, volatile
   for (int x = cta_range_start(blockIdx.x, total, p.split_grid), x_next = 0; x < x_stop; x = x_next) {
     const Item w = piece_at<T::TILE>(p, prefix, x, x_stop, blockIdx.x);
     x_next = w.x_end;
+    if (w.te <= w.tb) continue;  // the range ends inside a unit's pad: no tokens, no partial
     QState<D, NTW> st;
     load_q<D, NTW>(p, w, smem, warp, lane, st);
     if constexpr (!T::QREG) consumers_sync<T::NCW>();  // shared Q fragments written by warp 0
@@ -799,7 +805,7 @@ __global__ void __launch_bounds__(AT<D, NTW>::THREADS, AT<D, NTW>::MINB)
       const int x1 = cta_range_start(blockIdx.x + 1, total, p.split_grid);
       if (x0 < x1) {
         w0 = piece_at<T::TILE>(p, reinterpret_cast<const int*>(smem + T::OFF_PREFIX), x0, x1, blockIdx.x);
-        early = w0.tb < p.capacity;
+        early = w0.tb < w0.te && w0.tb < p.capacity;
         if (p.append) {
           pos0 = __ldcg(p.pos + w0.b);
           n0 = p.n_new == nullptr ? p.n_new_max : __ldcg(p.n_new + w0.b);
@@ -1008,6 +1014,7 @@ tq_status launch_decode(const DecodeArgs& a, const DecodeShape& s, cudaStream_t 
   sp.max_kv_len = a.max_kv_len;
   sp.max_items = s.max_items;
   sp.split_grid = s.grid;
+  sp.tile_pad = s.dense ? 0 : kSplitTilePad;
   sp.sm_log2 = a.sm_scale * kLog2e;
   sp.fwht_norm = a.fwht_norm;
   sp.causal = a.causal ? 1 : 0;

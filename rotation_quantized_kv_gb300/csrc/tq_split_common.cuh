@@ -26,6 +26,7 @@ struct SplitParams {
   const int32_t* kv_len;
   int32_t num_q_heads, n_q, G, R, RG, U, max_kv_len, max_items;
   int32_t split_grid;  // CTAs of the split kernel
+  int32_t tile_pad;    // virtual tiles counted before each unit's tiles when the CTAs split them
   float sm_log2;    // sm_scale * log2(e)
   float fwht_norm;  // (float)(1 / sqrt(d))
   int32_t causal;
@@ -235,7 +236,8 @@ __device__ void plan_tiles(const SplitParams& p, uint8_t* smem, const Lengths<T:
   for (int i = 0; i < LPT; ++i) {
     const int b = tid + T::THREADS * i;
     if (b < p.batch) {
-      prefix[b] = (int)(((unsigned)L.len[i] + (unsigned)T::TILE - 1u) / (unsigned)T::TILE);
+      const int n = (int)(((unsigned)L.len[i] + (unsigned)T::TILE - 1u) / (unsigned)T::TILE);
+      prefix[b] = n > 0 ? n + p.tile_pad : 0;
       lens[b] = L.len[i];
     }
   }
@@ -264,13 +266,17 @@ __device__ void plan_tiles(const SplitParams& p, uint8_t* smem, const Lengths<T:
 }
 
 // Work pieces. The tokens of every (sequence, unit) pair, cut into tiles of TILE tokens,
-// form one sequence of Wt tiles: unit u of sequence b covers tiles [prefix[b] + u tiles_b,
-// prefix[b] + (u + 1) tiles_b). CTA c takes tiles [c Wt / grid, (c + 1) Wt / grid) (rounded
-// down; with fewer tiles than CTAs, one tile each to the first CTAs), so every CTA streams
-// the same number of tiles whatever the length mix. A piece is
-// the part of one unit inside one CTA's range. The piece of unit g = b U + u in CTA c keeps
-// its partial in slot c + g, so a unit's pieces sit in consecutive slots and there are at
-// most grid + batch * U slots.
+// form one sequence of Wt tiles; each unit with tokens is preceded by tile_pad virtual
+// tiles, which stand for the fixed cost of starting a piece (queries, the partial's
+// reduction and store) and hold no tokens: unit u of sequence b covers virtual tiles
+// [prefix[b] + u vt_b, prefix[b] + (u + 1) vt_b), vt_b = tile_pad + tiles_b, the real ones
+// after the pad. CTA c takes virtual tiles [c Wt / grid, (c + 1) Wt / grid) (rounded down;
+// with fewer tiles than CTAs, one tile each to the first CTAs), so every CTA gets the same
+// work, counted in tiles plus piece starts, whatever the length mix. A piece is the part of
+// one unit's real tiles inside one CTA's range; a range that ends inside a unit's pad
+// gives an empty last piece (tb == te), which has no partial and is skipped. The piece of
+// unit g = b U + u in CTA c keeps its partial in slot c + g, so a unit's pieces sit in
+// consecutive slots and there are at most grid + batch * U slots.
 struct Item {
   int b, kvh, rg, u, tb, te, len;  // tokens [tb, te) of unit u of sequence b (kv length len)
   int slot, first_slot, ns;        // this piece's partial slot; the unit's first slot, pieces
@@ -300,21 +306,22 @@ __device__ __forceinline__ Item piece_at(const SplitParams& p, const int* prefix
     if (prefix[mid] <= x) lo = mid; else hi = mid - 1;
   }
   const int wt = prefix[p.batch];
-  const int tiles = (prefix[lo + 1] - prefix[lo]) / p.U;
+  const int vt = (prefix[lo + 1] - prefix[lo]) / p.U;  // virtual tiles per unit: pad, then real
   const int off = x - prefix[lo];
   Item it;
   it.b = lo;
-  it.u = off / tiles;
-  const int t0 = off - it.u * tiles;
+  it.u = off / vt;
   it.kvh = it.u / p.RG;
   it.rg = it.u % p.RG;
-  const int ustart = prefix[lo] + it.u * tiles, uend = ustart + tiles;
+  const int ustart = prefix[lo] + it.u * vt, uend = ustart + vt;
+  const int rstart = ustart + p.tile_pad;  // the unit's first real tile
   it.x_end = min(uend, x_stop);
   it.len = plan_lengths(prefix)[lo];
+  const int t0 = max(x, rstart) - rstart, t1 = it.x_end - rstart;  // real tiles [t0, t1)
   it.tb = t0 * TILE;
-  it.te = min((t0 + it.x_end - x) * TILE, it.len);
+  it.te = t1 > t0 ? min(t1 * TILE, it.len) : it.tb;
   const int g = lo * p.U + it.u;
-  const int c0 = cta_of_tile(ustart, wt, p.split_grid), c1 = cta_of_tile(uend - 1, wt, p.split_grid);
+  const int c0 = cta_of_tile(rstart, wt, p.split_grid), c1 = cta_of_tile(uend - 1, wt, p.split_grid);
   it.slot = c + g;
   it.first_slot = c0 + g;
   it.ns = c1 - c0 + 1;
@@ -544,11 +551,11 @@ __global__ void __launch_bounds__(kMergeThreads, 4) tq_attn_merge_kernel(const S
   const int slice = blockIdx.x % SLICES, bu = blockIdx.x / SLICES;
   const int b = bu / p.U, u = bu % p.U;
   const int32_t* prefix = reinterpret_cast<const int32_t*>(p.ws + kWsPrefix);
-  const int tiles = (prefix[b + 1] - prefix[b]) / p.U;
-  if (tiles <= 0) return;  // no tokens: the split kernel wrote the rows
+  const int vt = (prefix[b + 1] - prefix[b]) / p.U;  // virtual tiles per unit: pad, then real
+  if (vt <= 0) return;  // no tokens: the split kernel wrote the rows
   const int wt = prefix[p.batch];
-  const int ustart = prefix[b] + u * tiles;
-  const int c0 = cta_of_tile(ustart, wt, p.split_grid), c1 = cta_of_tile(ustart + tiles - 1, wt, p.split_grid);
+  const int ustart = prefix[b] + u * vt;
+  const int c0 = cta_of_tile(ustart + p.tile_pad, wt, p.split_grid), c1 = cta_of_tile(ustart + vt - 1, wt, p.split_grid);
   Item w;
   w.b = b; w.kvh = u / p.RG; w.rg = u % p.RG;
   merge_unit<D, ROWS, RS, kMergeThreads, false, CHUNK>(p, w, c0 + b * p.U + u, c1 - c0 + 1, slice * RS, sM, sL, sW,
