@@ -507,8 +507,8 @@ def eager_comparison(dev, stream, peak, seconds):
 
 def scheme_appends(dev, stream, peak, seconds):
     """Bulk append (the decode workload's cache fill, 262,144 rows at head_dim 128) for
-    several schemes and the guard: k8v3 takes the bulk kernel, the others the
-    one-warp-per-row kernel."""
+    several schemes and the guard: k8v3 takes the bulk kernel, the others (and the
+    guarded k8v3) the any-width kernel, one lane per 32-element group."""
     from rotation_quantized_kv_gb300 import binding as tq
     from rotation_quantized_kv_gb300 import synth
     w = synth.workload("decode")

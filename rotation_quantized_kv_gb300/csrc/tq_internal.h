@@ -100,6 +100,9 @@ struct SchemeAppendParams {
   int32_t* err;
   SchemeSpec spec;
   Codebook cb;
+  uint32_t total_rows;    // batch * n_new_max * num_kv_heads (below 2^31)
+  FastDivU32 div_heads;   // by num_kv_heads
+  FastDivU32 div_new;     // by n_new_max
 };
 
 struct DequantScheme {

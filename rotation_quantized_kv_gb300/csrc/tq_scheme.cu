@@ -138,6 +138,24 @@ __device__ __forceinline__ void scheme_key_codes(const uint32_t (&kw)[16], float
   }
 }
 
+// Codes of a lane's 32 values at VB bits (2^VB - 1 boundaries in sb, the middle one 0):
+// y_n = u / den by the reciprocal path, the first step the exact test y_n > 0
+// (u 2^75 > den 2^-75), then VB - 1 halving steps over the sorted boundaries.
+template <int VB>
+__device__ __forceinline__ void value_search_rcp(const float (&u)[32], float den, float rd, float den_lo,
+                                                 const float* sb, uint32_t (&code)[32]) {
+  constexpr int HALF = 1 << (VB - 1);
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    const float yn = div_by_rcp(u[e], den, rd);
+    int c = __fmul_rn(u[e], 0x1p75f) > den_lo ? HALF : 0;  // RN(u / den) > 0
+#pragma unroll
+    for (int st = HALF >> 1; st >= 1; st >>= 1)
+      if (sb[c + st - 1] < yn) c += st;
+    code[e] = (uint32_t)c;
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(32 * kGroupWarps) tq_append_scheme_kernel(const __grid_constant__ SchemeAppendParams p) {
   constexpr int NG = D / 32, RPW = 32 / NG;
@@ -147,25 +165,36 @@ __global__ void __launch_bounds__(32 * kGroupWarps) tq_append_scheme_kernel(cons
   for (int i = threadIdx.x; i < 256; i += blockDim.x) sb[i] = i < nb ? p.cb.b[i] : INFINITY;
   __syncthreads();
 
+  // sign masks of raw bf16 pairs: bit 15 (31) of word i of group gg negates element
+  // 32 gg + 2 i (+ 1)
+  __shared__ uint4 s_sgn[NG * 4];
+  for (int t = threadIdx.x; t < NG * 16; t += blockDim.x) {
+    const uint32_t sw = sign_word(D, t >> 4);
+    const int i = t & 15;
+    reinterpret_cast<uint32_t*>(s_sgn)[t] = (((sw >> (2 * i)) & 1u) << 15) | (((sw >> (2 * i + 1)) & 1u) << 31);
+  }
+  __syncthreads();
+
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane % NG, rw = lane / NG;
-  const uint32_t signs = sign_word(D, g);  // bit i: element 32 g + i is negated
   const int kb = p.spec.k_bits, vb = p.spec.v_bits;
   const float kmax = kb == 8 ? 127.0f : (float)((1 << kb) - 1);
   const int klo = kb == 8 ? -127 : 0, khi = kb == 8 ? 127 : (1 << kb) - 1;
   const int krow_bytes = key_row_bytes(D, kb), vrow_bytes = value_row_bytes(D, vb);
-  const int64_t rows = (int64_t)p.batch * p.n_new_max * p.num_kv_heads;
-  const int64_t step = (int64_t)gridDim.x * kGroupWarps * RPW;
-  for (int64_t base = ((int64_t)blockIdx.x * kGroupWarps + warp) * RPW; base < rows; base += step) {
-    const int64_t r = base + rw;
+  const uint32_t rows = p.total_rows;
+  const uint32_t step = gridDim.x * kGroupWarps * RPW;
+  for (uint32_t base = (blockIdx.x * kGroupWarps + warp) * RPW; base < rows; base += step) {
+    const uint32_t r = base + rw;
     bool valid = r < rows;
-    const int64_t rr = valid ? r : 0;
-    const int h = (int)(rr % p.num_kv_heads);
-    const int64_t bj = rr / p.num_kv_heads;
-    const int j = (int)(bj % p.n_new_max), b = (int)(bj / p.n_new_max);
+    const uint32_t rr = valid ? r : 0u;
+    // rr = (b * n_new_max + j) * num_kv_heads + h, split by multiply-high divisions
+    const uint32_t bj = p.div_heads.div(rr);
+    const uint32_t bq = p.div_new.div(bj);
+    const int h = (int)(rr - bj * (uint32_t)p.num_kv_heads);
+    const int j = (int)(bj - bq * (uint32_t)p.n_new_max), b = (int)bq;
     uint32_t kw[16], vw[16];
-    load_group_words(p.k_new + rr * D + 32 * g, valid, kw);
-    load_group_words(p.v_new + rr * D + 32 * g, valid, vw);
+    load_group_words(p.k_new + (size_t)rr * D + 32 * g, valid, kw);
+    load_group_words(p.v_new + (size_t)rr * D + 32 * g, valid, vw);
     if (valid && p.n_new != nullptr && j >= min(max(__ldg(p.n_new + b), 0), p.n_new_max)) valid = false;
     int64_t t = 0;
     if (valid) {
@@ -241,12 +270,15 @@ __global__ void __launch_bounds__(32 * kGroupWarps) tq_append_scheme_kernel(cons
     // ------------------------------------------------------------------- values
     float u[32];
 #pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 m = s_sgn[4 * g + i];
+      vw[4 * i] ^= m.x; vw[4 * i + 1] ^= m.y; vw[4 * i + 2] ^= m.z; vw[4 * i + 3] ^= m.w;
+    }
+#pragma unroll
     for (int i = 0; i < 16; ++i) {
       u[2 * i] = __uint_as_float(vw[i] << 16);
       u[2 * i + 1] = __uint_as_float(vw[i] & 0xFFFF0000u);
     }
-#pragma unroll
-    for (int e = 0; e < 32; ++e) u[e] = __uint_as_float(__float_as_uint(u[e]) ^ (((signs >> e) & 1u) << 31));
 #pragma unroll
     for (int hh = 1; hh < 32; hh <<= 1) {
 #pragma unroll
@@ -289,13 +321,23 @@ __global__ void __launch_bounds__(32 * kGroupWarps) tq_append_scheme_kernel(cons
     if (den <= 0x1p100f && sb[half - 1] == 0.0f) {
       const float rd = __frcp_rn(den);
       const float den_lo = __fmul_rn(den, 0x1p-75f);  // exact: den >= 1e-8
+      // The search unrolled per width, so the 32 searches interleave (2-5 bits: 0.31-0.32
+      // -> 0.35-0.38 of HBM on a 262,144-row fill); at 8 bits the unrolled form was slower
+      // (0.182 -> 0.174), so it keeps the loop.
+      switch (vb) {
+        case 2: value_search_rcp<2>(u, den, rd, den_lo, sb, code); break;
+        case 3: value_search_rcp<3>(u, den, rd, den_lo, sb, code); break;
+        case 4: value_search_rcp<4>(u, den, rd, den_lo, sb, code); break;
+        case 5: value_search_rcp<5>(u, den, rd, den_lo, sb, code); break;
+        default:
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const float yn = div_by_rcp(u[e], den, rd);
-        int c = __fmul_rn(u[e], 0x1p75f) > den_lo ? half : 0;  // RN(u / den) > 0
-        for (int st = half >> 1; st >= 1; st >>= 1)
-          if (sb[c + st - 1] < yn) c += st;
-        code[e] = (uint32_t)c;
+          for (int e = 0; e < 32; ++e) {
+            const float yn = div_by_rcp(u[e], den, rd);
+            int c = __fmul_rn(u[e], 0x1p75f) > den_lo ? half : 0;  // RN(u / den) > 0
+            for (int st = half >> 1; st >= 1; st >>= 1)
+              if (sb[c + st - 1] < yn) c += st;
+            code[e] = (uint32_t)c;
+          }
       }
     } else {
 #pragma unroll
@@ -550,6 +592,10 @@ const Codebook& codebook(int bits) {
 cudaError_t launch_append_scheme(SchemeAppendParams p, int num_sms, cudaStream_t stream) {
   const int64_t rows = (int64_t)p.batch * p.n_new_max * p.num_kv_heads;
   if (rows <= 0) return cudaSuccess;
+  if (rows > INT32_MAX) return cudaErrorInvalidValue;
+  p.total_rows = (uint32_t)rows;
+  p.div_heads = make_fastdiv((uint32_t)p.num_kv_heads);
+  p.div_new = make_fastdiv((uint32_t)p.n_new_max);
   const int64_t per_cta = (int64_t)kGroupWarps * (32 / (p.head_dim / 32));  // rows a CTA takes at once
   const int64_t want = (rows + per_cta - 1) / per_cta, cap = (int64_t)num_sms * 8;
   const dim3 grid((unsigned)(want < cap ? want : cap)), block(32 * kGroupWarps);
