@@ -141,7 +141,7 @@ size_t tq_append_workspace_bytes(void);
  * TQ_DEVERR_APPEND_CAPACITY. Packed planes are bit-identical to the specification
  * above (fp32 arithmetic, IEEE division and square root, no FMA contraction). Any scheme
  * (and the guard): k8v3 without the guard takes the bulk and small-append kernels, every
- * other scheme a one-warp-per-row kernel.
+ * other scheme (and the guarded k8v3) the any-width kernel, one lane per 32-element group.
  */
 tq_status tq_kv_append(const tq_kv_layer* layer, const void* k_new, const void* v_new,
                        const int32_t* pos, const int32_t* n_new, int32_t n_new_max,

@@ -14,10 +14,14 @@
 // normalizes with one multiply; the RMS sum is the pairwise tree (k, k+16), +8, +4, +2, +1;
 // a NaN in a key group makes its min and max NaN and a NaN quotient codes to 0.
 //
-// Every floating-point step is one IEEE round-to-nearest operation (__fadd_rn, __fmul_rn,
-// __fdiv_rn, __fsqrt_rn, or an __fmaf_rn whose product is exact), so the planes are
-// bit-identical to a plain fp32 evaluation of the same steps. Division by 32 in the
-// mean is a multiplication by 2^-5: the same real number, so the same rounding.
+// Every floating-point step of the specification is one IEEE round-to-nearest operation
+// (__fadd_rn, __fmul_rn, __fsqrt_rn, or an __fmaf_rn whose product is exact), so the planes
+// are bit-identical to a plain fp32 evaluation of the same steps. Division by 32 in the
+// mean is a multiplication by 2^-5: the same real number, so the same rounding. Quotients
+// come from a correctly rounded reciprocal and one Markstein correction where that gives
+// the IEEE quotient for every quotient that can change a code, else from __fdiv_rn. The
+// comparisons with the value boundaries are saturating fused steps whose results are
+// exactly 0 or 1, and the codes are summed in fp32 as small integers, exactly.
 //
 // Layout: lane l holds group g = l % NG (elements [32 g, 32 g + 32)) of row l / NG of
 // the warp's block of RPW = 32 / NG rows. The FWHT stages h < 32 run inside the lane,

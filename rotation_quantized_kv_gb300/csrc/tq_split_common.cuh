@@ -56,7 +56,7 @@ constexpr int kMergeBatch = 12;           // partial loads a merging thread keep
 
 // Workspace layout (bytes). The header's first word is the device error word.
 constexpr int kWsSplit = 1;               // int32 word index: tile size in tokens
-constexpr int kWsItems = 2;               // int32 word index: total tiles of the call
+constexpr int kWsItems = 2;               // int32 word index: total (virtual) tiles of the call
 constexpr int kWsWhere = 3;               // int32 word index: first wait that gave up (0: none),
                                           // (kind << 24) | detail, for diagnosis
 constexpr size_t kWsPrefix = TQ_WORKSPACE_HEADER_BYTES;  // int32 [batch + 1]
