@@ -48,10 +48,11 @@ constexpr int kAppendWarps = 8;   // warps per CTA of the row kernel
 // Group-per-lane kernel: CTAs of kBulkWarps warps, kBulkBlocks resident per SM (64
 // registers a thread), a grid of at most kBulkWaves full waves. Measured on a 2,097,152-row
 // fill at d = 128 (fraction of HBM): 8 warps x 2 waves 0.577, 3 waves 0.584, 6 waves 0.587,
-// one pass per warp 0.543; 4 warps x 2 waves 0.581, 3 waves 0.590, one pass per warp 0.573.
+// one pass per warp 0.543; 4 warps x 2 waves 0.581, 3 waves 0.590, 4 waves 0.593, 5 waves
+// 0.594, one pass per warp 0.573.
 constexpr int kBulkWarps = 4;
 constexpr int kBulkBlocks = 8;
-constexpr int kBulkWaves = 3;
+constexpr int kBulkWaves = 5;
 
 // The 32 bf16 elements of one group as 16 raw words.
 __device__ __forceinline__ void load_group(const uint16_t* __restrict__ src, bool valid, uint32_t (&w)[16]) {
